@@ -1,0 +1,204 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library
+ * (libpagedattn.so).
+ *
+ * The library implements the composition a model layer performs on its KV
+ * cache: a slot-mapped write of each new token's K and V into a pool of
+ * 16-token pages, then grouped-query causal softmax attention that reads the
+ * pool back through a per-request block table, for full prefill, suffix
+ * (chunked) prefill and single-query decode.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [C] "test(rocm): ReshapeAndCache->PagedAttention composition at real dims"
+ *       -- What changed; maintainer review and rework (slot mapping derived
+ *       from the block table, anti-vacuity guard).
+ *   [R] "fix(rocm): stabilize direct paged CK attention for bitwise R/R"
+ *       -- intro and Changes (fixed arithmetic schedule, real maximum query
+ *       length, no implicit FMA contraction, tail-page sanitising, 64-bit
+ *       addressing, one query per decode row, graph-cache identity including
+ *       the KV scheduling bound); Additional checks (bitwise matrix).
+ *
+ * Conventions shared by every entry point:
+ *   - All device buffers are owned by the caller.  The library never
+ *     allocates device memory, never synchronises the stream (except
+ *     pa_check_errors) and never reads device memory on the host, so calls
+ *     are asynchronous on `stream` and can be captured in a CUDA graph.
+ *   - Element types: q, key, value, caches and out are BF16 (passed as
+ *     void*); slot_mapping is int64; block tables, lengths and
+ *     query_start_loc are int32; lse is fp32.
+ *   - Strides are in ELEMENTS; the head dimension is always contiguous.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failing check returns a status and launches nothing.  There is no
+ *     fallback path: an unsupported shape is an error.
+ *   - Device-side metadata errors (a block id outside [0, num_blocks), a slot
+ *     past the pool, seq_len < query length, a non-monotone query_start_loc)
+ *     never fault: the affected rows are written as NaN (attention) or
+ *     skipped (cache write), other rows are untouched, and the first error
+ *     is latched in a device flag read by pa_check_errors.
+ *   - `stream` is a cudaStream_t (0 = legacy default stream).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad stride */
+    PA_ERR_UNSUPPORTED = 2,  /* shape outside the supported set (see below) */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    PA_ERR_BAD_METADATA = 4, /* device-side metadata error (pa_check_errors) */
+    PA_ERR_TIMEOUT = 5,      /* an in-kernel wait ran past its limit */
+    PA_ERR_CUDA = 6          /* a CUDA runtime call failed */
+} pa_status;
+
+/*
+ * One paged KV cache: a K view and a V view with one shared set of strides.
+ * Element (block, token-in-block, kv-head, d) of K is at
+ *   k + block*block_stride + token*token_stride + head*head_stride + d.
+ * The pages' pools map onto it as follows ([R] Additional checks names the
+ * "separate", "interleaved" and ">2 GB" layouts):
+ *   separate    : K and V are two [num_blocks, 16, Hkv, Dh] tensors;
+ *   interleaved : one [num_blocks, 2, 16, Hkv, Dh] tensor, K = [:,0], V = [:,1]
+ *                 (block_stride = 2*16*Hkv*Dh).
+ * Offsets are computed in 64 bits, so a view may exceed 2**31 elements.
+ * Requirements: block_size == 16; head_dim in {128, 256, 512}; k and v
+ * 16-byte aligned; every stride a multiple of 8 elements (16 bytes).
+ */
+typedef struct {
+    void *k;
+    void *v;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t reserved; /* set to 0 */
+    int64_t block_stride;
+    int64_t token_stride;
+    int64_t head_stride;
+} pa_kv_cache;
+
+/*
+ * Sets kernel attributes (dynamic shared memory) for the current device.
+ * Called implicitly by the first launch on a device; call it explicitly
+ * before capturing a CUDA graph ([R] Changes: warm before graph capture).
+ */
+PA_API pa_status pa_init(void);
+
+/*
+ * ReshapeAndCache ([C] What changed and review rework).  For every token i
+ * in [0, num_tokens) with slot = slot_mapping[i] >= 0, copies the Dh BF16
+ * values of each KV head h from key[i][h][:] and value[i][h][:] into block
+ * slot/16, offset slot%16, head h of the K and V views.  A negative slot
+ * marks a padding token and is skipped.  A slot >= num_blocks*16 is not
+ * written and latches PA_ERR_BAD_METADATA with first_bad_index = i.
+ *   key, value        : [num_tokens, Hkv, Dh] BF16, token stride
+ *                       key_tok_stride / value_tok_stride (elements, >= Hkv*Dh,
+ *                       multiple of 8), heads contiguous; 16-byte aligned.
+ *   slot_mapping      : [num_tokens] int64 on the device.
+ *   cache             : host struct describing the device pool (read only).
+ * Duplicate non-negative slots are undefined (the pages' mapping never makes
+ * them).  num_tokens == 0 launches nothing.
+ */
+PA_API pa_status pa_reshape_and_cache(const void *key, int64_t key_tok_stride, const void *value,
+                               int64_t value_tok_stride, int64_t num_tokens,
+                               const pa_kv_cache *cache, const int64_t *slot_mapping,
+                               pa_stream_t stream);
+
+/*
+ * Bytes of scratch that pa_paged_attention needs for these bounds (split-KV
+ * partial states and arrival counters).  The same bounds must be passed to
+ * pa_paged_attention.  Returns 0 for invalid arguments.
+ */
+PA_API size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t max_query_len, int32_t max_seq_len);
+
+/*
+ * PagedAttention ([C] What changed; [R] Changes and Additional checks).
+ * For request b (0 <= b < num_seqs) with q_b = query_start_loc[b+1] -
+ * query_start_loc[b] new tokens and L_b = seq_lens[b] cached tokens (the new
+ * tokens included, already written by pa_reshape_and_cache), query i of the
+ * request sits at position p = L_b - q_b + i and attends causally to keys
+ * 0..p.  Query head h uses KV head h / (Hq/Hkv).  Key j of request b lives
+ * in block block_tables[b*max_blocks_per_seq + j/16] at offset j%16; table
+ * columns at or past ceil(L_b/16) are never read.
+ *   out[t][h][:] = softmax_j(scale * q[t][h].K_j) . V_j   (BF16, RNE)
+ *   lse[t][h]    = ln(sum_j exp(scale * q[t][h].K_j))     (fp32, may be NULL)
+ * Decode is query_start_loc = {0, 1, ..., num_seqs} ([R] Changes: one query
+ * per row of metadata).
+ *
+ *   q                 : [num_q_tokens, Hq, Dh] BF16, token stride q_tok_stride
+ *                       (elements, >= Hq*Dh, multiple of 8), heads contiguous.
+ *   out               : [num_q_tokens, Hq, Dh] BF16, contiguous.  Rows of
+ *                       tokens owned by no request are left untouched.
+ *   lse               : [num_q_tokens, Hq] fp32, contiguous, or NULL.
+ *   block_tables      : [num_seqs, max_blocks_per_seq] int32.
+ *   seq_lens          : [num_seqs] int32.  query_start_loc: [num_seqs+1] int32,
+ *                       non-decreasing, last entry <= num_q_tokens.
+ *   max_query_len, max_seq_len : host-side upper bounds of q_b and L_b.  They
+ *                       size the grid and the workspace only; any valid bound
+ *                       gives bitwise-identical results ([R] Changes: real
+ *                       maximum query length; KV scheduling bound in the graph
+ *                       identity).  A request exceeding them latches
+ *                       PA_ERR_BAD_METADATA.
+ *   scale             : softmax scale (typically 1/sqrt(Dh)).
+ *   workspace         : device scratch of at least
+ *                       pa_paged_attention_workspace_size(...) bytes, 256-byte
+ *                       aligned, zero-filled before its first use; the library
+ *                       leaves it ready for the next call.  One workspace must
+ *                       not be used by two calls that may run concurrently.
+ * Supported: head_dim in {128, 256, 512}; Hq % Hkv == 0; Hq/Hkv <= 128.
+ *
+ * Arithmetic is fixed ([R] intro: one schedule for strict agreement): every
+ * (token, head) row is computed by the same sequence of operations whatever
+ * the batch, the other requests, the query length or the bounds, so a
+ * token's output and lse are bitwise identical in full prefill, suffix
+ * prefill and decode.
+ */
+PA_API pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_stride,
+                             int32_t num_q_heads, const pa_kv_cache *cache,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *seq_lens, const int32_t *query_start_loc,
+                             int32_t num_seqs, int32_t max_query_len, int32_t max_seq_len,
+                             float scale, void *out, float *lse, void *workspace,
+                             size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * flag.  Returns PA_OK, PA_ERR_BAD_METADATA or PA_ERR_TIMEOUT (or
+ * PA_ERR_CUDA if the synchronisation failed).  *first_bad_index (may be
+ * NULL) receives the token index (cache write) or request index (attention)
+ * of the first recorded error, else -1.
+ */
+PA_API pa_status pa_check_errors(pa_stream_t stream, int64_t *first_bad_index);
+
+/* Static, human-readable name of a status code. */
+PA_API const char *pa_status_string(pa_status status);
+
+/*
+ * Copies a one-line description of the calling thread's most recent launch
+ * (schedule, grid, chunk count, KV tile) into buf (NUL-terminated,
+ * truncated to n bytes) -- the "selected entrypoint" breadcrumb of
+ * [R] Changes.
+ */
+PA_API void pa_last_launch_info(char *buf, size_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

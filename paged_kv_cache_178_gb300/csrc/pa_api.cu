@@ -1,0 +1,304 @@
+// C-ABI front end of libpagedattn.so: argument validation, the cache write
+// kernel (K1), the device error latch and launch breadcrumbs.  The attention
+// kernel lives in pa_attn.cu.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedattn.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One error latch per device (each device that loads the module has its own
+// copy); host code reaches it through cudaGetSymbolAddress.
+__device__ ErrState g_err_state;
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_mu;
+static ErrState *g_err_ptr[kMaxDevices];
+static bool g_attr_done[kMaxDevices];
+static thread_local char g_last_info[256] = "none";
+
+static pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Per-device one-time set-up: resolve the error latch address and set kernel
+// attributes.  Must run with the device current.
+static pa_status device_setup(ErrState **err_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_attr_done[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_err_state) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (init_attention_attributes() != cudaSuccess)
+            return PA_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<ErrState *>(ptr);
+        g_attr_done[dev] = true;
+    }
+    if (err_out)
+        *err_out = g_err_ptr[dev];
+    return PA_OK;
+}
+
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
+                      const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                      CUtensorMapSwizzle swizzle)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn)
+        return CUDA_ERROR_NOT_FOUND;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    return fn(map, dtype, rank, base, dims, strides_bytes, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// K1: slot-mapped cache write.  One thread per 16-byte vector of one
+// (token, kv head, K-or-V) row.  Offsets are 64-bit.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+    const uint4 *__restrict__ key, int64_t key_tok_stride, const uint4 *__restrict__ value,
+    int64_t value_tok_stride, int64_t num_tokens, int32_t num_kv_heads, int32_t vecs_per_row,
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots, int64_t block_stride,
+    int64_t token_stride, int64_t head_stride, const int64_t *__restrict__ slot_mapping, ErrState *err)
+{
+    // strides arrive in 16-byte units
+    const int64_t total = num_tokens * num_kv_heads * 2 * vecs_per_row;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int vec = (int)(idx % vecs_per_row);
+        int64_t rest = idx / vecs_per_row;
+        const int which = (int)(rest % 2);
+        rest /= 2;
+        const int h = (int)(rest % num_kv_heads);
+        const int64_t i = rest / num_kv_heads;
+        const int64_t slot = __ldg(slot_mapping + i);
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {
+            if (vec == 0 && which == 0 && h == 0)
+                record_error(err, kErrBadMetadata, i);
+            continue;
+        }
+        const int64_t dst = (slot >> 4) * block_stride + (slot & 15) * token_stride + h * head_stride + vec;
+        if (which == 0)
+            k_cache[dst] = __ldg(key + i * key_tok_stride + (int64_t)h * vecs_per_row + vec);
+        else
+            v_cache[dst] = __ldg(value + i * value_tok_stride + (int64_t)h * vecs_per_row + vec);
+    }
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static pa_status check_cache(const pa_kv_cache *c)
+{
+    if (!c || !c->k || !c->v)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(c->k) || !aligned16(c->v))
+        return PA_ERR_INVALID_ARG;
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (c->block_size != 16)
+        return PA_ERR_UNSUPPORTED;
+    if (c->head_dim != 128 && c->head_dim != 256 && c->head_dim != 512)
+        return PA_ERR_UNSUPPORTED;
+    if (c->block_stride <= 0 || c->token_stride <= 0 || c->head_stride <= 0)
+        return PA_ERR_INVALID_ARG;
+    if ((c->block_stride | c->token_stride | c->head_stride) & 7)
+        return PA_ERR_INVALID_ARG;
+    if (c->head_stride < c->head_dim || c->num_blocks > (int64_t)1 << 31)
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+extern "C" {
+
+const char *pa_status_string(pa_status s)
+{
+    switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_BAD_METADATA: return "PA_ERR_BAD_METADATA";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+void pa_last_launch_info(char *buf, size_t n)
+{
+    if (!buf || !n)
+        return;
+    snprintf(buf, n, "%s", g_last_info);
+}
+
+pa_status pa_init(void) { return device_setup(nullptr); }
+
+pa_status pa_reshape_and_cache(const void *key, int64_t key_tok_stride, const void *value,
+                               int64_t value_tok_stride, int64_t num_tokens, const pa_kv_cache *cache,
+                               const int64_t *slot_mapping, pa_stream_t stream)
+{
+    pa_status st = check_cache(cache);
+    if (st != PA_OK)
+        return st;
+    if (num_tokens < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) {
+        snprintf(g_last_info, sizeof g_last_info, "reshape_and_cache tokens=0 (nothing launched)");
+        return PA_OK;
+    }
+    const int64_t row = (int64_t)cache->num_kv_heads * cache->head_dim;
+    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
+        return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return PA_ERR_INVALID_ARG;
+    if (key_tok_stride < row || value_tok_stride < row || (key_tok_stride & 7) || (value_tok_stride & 7))
+        return PA_ERR_INVALID_ARG;
+    ErrState *err = nullptr;
+    if ((st = device_setup(&err)) != PA_OK)
+        return st;
+    const int vecs = cache->head_dim / 8;
+    const int64_t total = num_tokens * cache->num_kv_heads * 2 * vecs;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16)
+        blocks = 152 * 16;
+    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(key), key_tok_stride / 8, static_cast<const uint4 *>(value),
+        value_tok_stride / 8, num_tokens, cache->num_kv_heads, vecs, static_cast<uint4 *>(cache->k),
+        static_cast<uint4 *>(cache->v), cache->num_blocks * 16, cache->block_stride / 8,
+        cache->token_stride / 8, cache->head_stride / 8, slot_mapping, err);
+    snprintf(g_last_info, sizeof g_last_info, "reshape_and_cache tokens=%lld grid=%lld block=256",
+             (long long)num_tokens, (long long)blocks);
+    return cuda_status(cudaGetLastError());
+}
+
+size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t max_query_len, int32_t max_seq_len)
+{
+    AttnPlan pl;
+    if (!plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, max_query_len, max_seq_len, &pl))
+        return 0;
+    return pl.ws_bytes;
+}
+
+pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_stride, int32_t num_q_heads,
+                             const pa_kv_cache *cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                             int32_t max_query_len, int32_t max_seq_len, float scale, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, pa_stream_t stream)
+{
+    pa_status st = check_cache(cache);
+    if (st != PA_OK)
+        return st;
+    if (num_q_heads <= 0 || num_seqs < 0 || max_query_len < 0 || max_seq_len < 0 || num_q_tokens < 0 ||
+        max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % cache->num_kv_heads != 0 || num_q_heads / cache->num_kv_heads > 128)
+        return PA_ERR_UNSUPPORTED;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_q_tokens == 0 || max_query_len == 0) {
+        snprintf(g_last_info, sizeof g_last_info, "attention: empty batch (nothing launched)");
+        return PA_OK;
+    }
+    const int64_t row = (int64_t)num_q_heads * cache->head_dim;
+    if (!q || !out || !block_tables || !seq_lens || !query_start_loc || !aligned16(q) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return PA_ERR_INVALID_ARG;
+    if (q_tok_stride < row || (q_tok_stride & 7) || num_q_tokens > ((int64_t)1 << 31) - 1)
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq == 0)
+        return PA_ERR_INVALID_ARG;
+    AttnPlan pl;
+    if (!plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
+                        &pl))
+        return PA_ERR_UNSUPPORTED;
+    if (cache->head_dim == 512)
+        return PA_ERR_UNSUPPORTED;
+    if (pl.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < pl.ws_bytes)
+            return PA_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return PA_ERR_INVALID_ARG;
+    }
+    ErrState *err = nullptr;
+    if ((st = device_setup(&err)) != PA_OK)
+        return st;
+    AttnArgs a;
+    a.q = q;
+    a.num_q_tokens = num_q_tokens;
+    a.q_tok_stride = q_tok_stride;
+    a.num_q_heads = num_q_heads;
+    a.k = cache->k;
+    a.v = cache->v;
+    a.num_blocks = cache->num_blocks;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.head_dim = cache->head_dim;
+    a.block_stride = cache->block_stride;
+    a.token_stride = cache->token_stride;
+    a.head_stride = cache->head_stride;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.query_start_loc = query_start_loc;
+    a.num_seqs = num_seqs;
+    a.max_query_len = max_query_len;
+    a.max_seq_len = max_seq_len;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    cudaError_t e = launch_attention(a, pl, err, reinterpret_cast<cudaStream_t>(stream), g_last_info,
+                                     sizeof g_last_info);
+    if (e == cudaErrorNotSupported)
+        return PA_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+pa_status pa_check_errors(pa_stream_t stream, int64_t *first_bad_index)
+{
+    if (first_bad_index)
+        *first_bad_index = -1;
+    ErrState *err = nullptr;
+    pa_status st = device_setup(&err);
+    if (st != PA_OK)
+        return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    ErrState h{};
+    if (cudaMemcpy(&h, err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (h.code == 0)
+        return PA_OK;
+    const ErrState zero{};
+    if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (first_bad_index)
+        *first_bad_index = h.index;
+    return h.code == kErrTimeout ? PA_ERR_TIMEOUT : PA_ERR_BAD_METADATA;
+}
+
+}  // extern "C"

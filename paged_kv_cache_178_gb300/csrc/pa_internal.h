@@ -1,0 +1,82 @@
+// Internal interface between the C-ABI front end (pa_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Device-side error latch: the first error code and the index it concerns.
+struct ErrState {
+    unsigned int code;
+    unsigned int pad;
+    long long index;
+};
+
+enum : unsigned int { kErrBadMetadata = 4u, kErrTimeout = 5u };
+
+__device__ __forceinline__ void record_error(ErrState *e, unsigned int code, long long index)
+{
+    if (atomicCAS(&e->code, 0u, code) == 0u)
+        atomicExch(reinterpret_cast<unsigned long long *>(&e->index),
+                   static_cast<unsigned long long>(index));
+}
+
+// Validated, host-side description of one attention call.
+struct AttnArgs {
+    const void *q;
+    int64_t num_q_tokens;
+    int64_t q_tok_stride;
+    int32_t num_q_heads;
+    const void *k;
+    const void *v;
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int64_t block_stride, token_stride, head_stride;
+    const int32_t *block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;
+    const int32_t *query_start_loc;
+    int32_t num_seqs;
+    int32_t max_query_len;
+    int32_t max_seq_len;
+    float scale;
+    void *out;
+    float *lse;
+    void *workspace;
+    size_t workspace_bytes;
+};
+
+// Work decomposition chosen from host scalars only.
+struct AttnPlan {
+    int head_dim;
+    int group;          // Hq / Hkv
+    int tokens_per_tile;  // query tokens per 128-row tile
+    int qtiles;         // grid extent over query tiles
+    int nch;            // grid extent over KV chunks (1 unless split)
+    bool split;         // split-KV with partial states + in-kernel merge
+    int ws_rows;        // rows per partial-state record
+    size_t ws_counter_bytes;
+    size_t ws_bytes;    // total workspace needed
+    long long grid;     // CTAs (or clusters x 2 for Dh=512)
+};
+
+bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t max_query_len, int32_t max_seq_len, AttnPlan *plan);
+
+// Launch the attention kernel for a validated call.  Returns a CUDA error
+// code; *unsupported is set when the shape has no kernel.
+cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &plan, ErrState *err,
+                             cudaStream_t stream, char *info, size_t info_len);
+
+cudaError_t init_attention_attributes();
+
+// Encodes a tiled tensor map (driver entry point fetched at run time).
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
+                      const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                      const cuuint32_t *box, CUtensorMapSwizzle swizzle);
+
+}  // namespace pa

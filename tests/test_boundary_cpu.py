@@ -1,0 +1,123 @@
+"""The C-ABI boundary without a GPU: the library builds and loads, exports
+every entry point the header declares, and rejects bad arguments on the
+host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_178_gb300 import build as pa_build
+from paged_kv_cache_178_gb300 import pagedattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return pagedattn.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    assert set(pagedattn.EXPORTED) <= set(names)
+    assert "pa_reshape_and_cache" in names and "pa_paged_attention" in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED",
+                                 "PA_ERR_WORKSPACE", "PA_ERR_BAD_METADATA", "PA_ERR_TIMEOUT",
+                                 "PA_ERR_CUDA"]):
+        assert pagedattn.status_string(code) == name
+
+
+FAKE = 0x10000000  # aligned, never dereferenced: validation fails before any CUDA call
+
+
+def _cache(**kw):
+    c = dict(k=FAKE, v=FAKE + 0x1000, num_blocks=2048, block_size=16, num_kv_heads=2, head_dim=128,
+             reserved=0, block_stride=2 * 16 * 2 * 128, token_stride=2 * 128, head_stride=128)
+    c.update(kw)
+    return pagedattn.PaKvCache(**c)
+
+
+def _rc(lib, cache, key=FAKE, value=FAKE, kstride=256, vstride=256, n=4, slots=FAKE):
+    return lib.pa_reshape_and_cache(key, kstride, value, vstride, n, ctypes.byref(cache), slots, None)
+
+
+def test_cache_write_validation(lib):
+    assert _rc(lib, _cache(block_size=8)) == pagedattn.PA_ERR_UNSUPPORTED
+    assert _rc(lib, _cache(head_dim=64)) == pagedattn.PA_ERR_UNSUPPORTED
+    assert _rc(lib, _cache(k=FAKE + 2)) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(token_stride=250)) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(num_blocks=0)) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(), key=FAKE + 8) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(), kstride=128) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(), slots=FAKE + 4) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(), n=-1) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rc(lib, _cache(), n=0) == pagedattn.PA_OK          # nothing to launch
+    assert lib.pa_reshape_and_cache(FAKE, 256, FAKE, 256, 4, None, FAKE, None) == \
+        pagedattn.PA_ERR_INVALID_ARG
+
+
+def _attn(lib, cache, q=FAKE, ntok=4, qstride=1024, hq=8, bt=FAKE, maxblk=448, sl=FAKE, qsl=FAKE,
+          nseq=4, mq=1, ms=7168, scale=0.088, out=FAKE, lse=0, ws=0, ws_len=0):
+    return lib.pa_paged_attention(q, ntok, qstride, hq, ctypes.byref(cache), bt, maxblk, sl, qsl, nseq,
+                                  mq, ms, ctypes.c_float(scale), out, lse, ws, ws_len, None)
+
+
+def test_attention_validation(lib):
+    c = _cache()
+    ws = pagedattn.workspace_size(4, 8, 2, 128, 1, 7168)
+    assert _attn(lib, c, hq=7) == pagedattn.PA_ERR_UNSUPPORTED           # Hq % Hkv
+    assert _attn(lib, c, hq=2 * 129) == pagedattn.PA_ERR_UNSUPPORTED     # group > 128
+    assert _attn(lib, c, q=FAKE + 2) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, qstride=1000) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, out=0) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, lse=FAKE + 2) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, scale=float("nan")) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, ws=0, ws_len=0) == pagedattn.PA_ERR_WORKSPACE
+    assert _attn(lib, c, ws=FAKE, ws_len=ws - 1) == pagedattn.PA_ERR_WORKSPACE
+    assert _attn(lib, c, ws=FAKE + 16, ws_len=ws) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, nseq=0) == pagedattn.PA_OK                        # empty batch
+    assert _attn(lib, c, mq=-1) == pagedattn.PA_ERR_INVALID_ARG
+
+
+def test_workspace_size_is_host_arithmetic(lib):
+    # decode: 4 requests x 2 KV heads, one 4-row query tile each, 28 chunks
+    # of 256 keys, records of (m, l, O[128]) per row + 256 B of counters
+    assert pagedattn.workspace_size(4, 8, 2, 128, 1, 7168) == 256 + 8 * 28 * 4 * 130 * 4
+    # a long prefill runs in-CTA: no scratch at all
+    assert pagedattn.workspace_size(1, 8, 2, 128, 4096, 4096) == 0
+    # short sequences fit one chunk: no scratch
+    assert pagedattn.workspace_size(4, 8, 2, 128, 1, 256) == 0
+    # invalid geometry
+    assert pagedattn.workspace_size(4, 8, 3, 128, 1, 7168) == 0
+
+
+def test_no_gpu_calls_report_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    idx = ctypes.c_int64(7)
+    assert lib.pa_check_errors(None, ctypes.byref(idx)) == pagedattn.PA_ERR_CUDA
+    assert lib.pa_init() == pagedattn.PA_ERR_CUDA
+    assert _rc(lib, _cache()) == pagedattn.PA_ERR_CUDA
+
+
+def test_launch_info_is_a_string(lib):
+    s = pagedattn.last_launch_info()
+    assert isinstance(s, str) and len(s) > 0

@@ -1,0 +1,278 @@
+"""K2 (pa_paged_attention) against the fp64 oracle, and GPU-vs-GPU bitwise
+properties.
+
+Tolerances: out max-abs <= 2e-2 and lse relative <= 1e-3 against the oracle
+for N(0,1) inputs; prefill vs decode and schedule changes bit-exact ("fix(rocm):
+stabilize direct paged CK attention for bitwise R/R", Validation:
+mismatch_count=0, max_abs_diff=0, torch.equal=true; Additional checks)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_178_gb300 import pagedattn
+from paged_kv_cache_178_gb300 import workloads as wl
+from paged_kv_cache_178_gb300.device import DeviceWorkload
+from tests.helpers import LSE_RTOL, OUT_ATOL, lse_rel_err, oracle_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, **kw):
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention(**kw)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1), pagedattn.last_launch_info()
+    return dw, out, lse
+
+
+def _compare(w, out, lse, rows=None, compact=False, tag=""):
+    ref_o, ref_l = oracle_attention(w, rows=rows, compact=compact)
+    o = out.float().cpu().numpy()
+    l_ = lse.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        o, l_ = o[rows], l_[rows]
+    assert np.isfinite(o).all() and np.isfinite(l_).all()
+    err_o = float(np.max(np.abs(o - ref_o)))
+    err_l = lse_rel_err(l_, ref_l)
+    print(f"{w.name}{tag}: out max_abs_diff={err_o:.3e} lse rel={err_l:.3e} "
+          f"[{pagedattn.last_launch_info()}]")
+    assert err_o <= OUT_ATOL
+    assert err_l <= LSE_RTOL
+
+
+def _bitwise(a: torch.Tensor, b: torch.Tensor, what: str):
+    ai = a.contiguous().view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32)
+    bi = b.contiguous().view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)
+    mism = int((ai != bi).sum())
+    diff = float((a.float() - b.float()).abs().max()) if a.numel() else 0.0
+    print(f"{what}: mismatch_count={mism} max_abs_diff={diff} torch.equal={mism == 0}")
+    assert mism == 0
+
+
+def _rows_sample(n, extra=(), k=96, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    base = {0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 1023, 1024, n - 2, n - 1} | set(extra)
+    base |= set(torch.randint(0, n, (k,), generator=g).tolist())
+    return sorted(r for r in base if 0 <= r < n)
+
+
+# ------------------------------------------------------------- parity ----
+
+def test_composition_dh256():
+    w = wl.composition()
+    dw, out, lse = _run(w)
+    _compare(w, out, lse)
+    # closed form on the GPU too: row 0 sees one key, so out = v0 bit for bit
+    v0 = w.value[0].cuda()
+    for h in range(8):
+        assert torch.equal(out[0, h], v0[h // 4])
+
+
+def test_composition_anti_vacuity():
+    """Swapping two in-range logical blocks after the write changes the GPU
+    output (the composition review's guard); rows 0..3 then read only
+    written slots and still match the oracle run on the swapped table."""
+    w = wl.composition()
+    dw, out, _ = _run(w)
+    bt = w.block_table.clone()
+    bt[0, [0, 1]] = bt[0, [1, 0]]
+    out2, _ = dw.attention(block_tables=bt.cuda())
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    assert float((out2[:4].float() - out[:4].float()).abs().max()) > 1e-3
+    ref_o, _ = oracle_attention(dataclasses.replace(w, block_table=bt), rows=[0, 1, 2, 3])
+    assert float(np.max(np.abs(out2[:4].float().cpu().numpy() - ref_o))) <= OUT_ATOL
+
+
+@pytest.mark.parametrize("reversed_pages", [False, True])
+def test_decode(reversed_pages):
+    w = wl.decode(reversed_pages=reversed_pages)
+    dw, out, lse = _run(w)
+    _compare(w, out, lse)
+
+
+def test_decode_separate_layout():
+    w = dataclasses.replace(wl.decode(), layout="separate")
+    dw, out, lse = _run(w)
+    _compare(w, out, lse)
+
+
+def test_long_prefill_sampled():
+    w = wl.long_prefill(4096)
+    dw, out, lse = _run(w)
+    _compare(w, out, lse, rows=_rows_sample(4096, extra=(2047, 2048, 4094)))
+
+
+@pytest.mark.parametrize("qlen", [128, 17, 1])
+def test_suffix_over_4gb_pool(qlen):
+    w = wl.suffix(qlen)
+    dw, out, lse = _run(w)
+    rows = None if qlen <= 17 else _rows_sample(4 * qlen, k=64)
+    _compare(w, out, lse, rows=rows, compact=True, tag=f" q={qlen}")
+
+
+def test_mixed_batch_small_dims():
+    """Prefill, suffix and decode requests in one call, partial pages."""
+    gen = torch.Generator().manual_seed(31)
+    lens = [300, 16, 700, 1, 29, 513]
+    qlens = [300, 16, 9, 1, 1, 40]
+    pages = torch.randperm(200, generator=gen).tolist()
+    rows, at = [], 0
+    for L in lens:
+        n = wl.pages_needed(L)
+        rows.append(pages[at:at + n])
+        at += n
+    w = wl.build("mixed_dh128", num_q_heads=8, num_kv_heads=2, head_dim=128, seq_lens=lens,
+                 query_lens=qlens, num_blocks=200, block_rows=rows, layout="interleaved", seed=32)
+    dw, out, lse = _run(w)
+    _compare(w, out, lse)
+
+
+# ------------------------------------------------ prefill == decode bitwise ----
+
+def _prefill_vs_decode(w, rows):
+    dw, out, lse = _run(w)
+    wd = wl.decode_batch_from_prefill(w, rows)
+    dd = DeviceWorkload(wd, fill_bits=None)
+    dd.share_cache_with(dw)
+    out_d, lse_d = dd.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    qoff = int(w.query_start_loc[0])
+    idx = torch.tensor([qoff + r for r in rows], device=out.device)
+    _bitwise(out.index_select(0, idx), out_d, f"{w.name} out prefill vs decode ({len(rows)} rows; {info})")
+    _bitwise(lse.index_select(0, idx), lse_d, f"{w.name} lse prefill vs decode")
+    return info
+
+
+def test_long_prefill_equals_decode_all_rows():
+    w = wl.long_prefill(4096)
+    _prefill_vs_decode(w, list(range(4096)))
+
+
+def test_long_prefill_equals_split_decode():
+    """A small decode batch runs the split-KV schedule (chunk partials merged
+    by the last CTA); it must still equal the prefill rows bit for bit."""
+    w = wl.long_prefill(4096)
+    info = _prefill_vs_decode(w, [4095, 4000, 2048, 1023, 700, 255, 16, 0])
+    assert "split" in info
+
+
+@pytest.mark.parametrize("qlen", [128, 17])
+def test_suffix_equals_decode(qlen):
+    w = wl.suffix(qlen, num_blocks=4096)
+    # one request at a time: the decode view wants a single-request prefill
+    for b in (0, 3):
+        q0, q1 = int(w.query_start_loc[b]), int(w.query_start_loc[b + 1])
+        kv0 = sum(int(x) for x in w.seq_lens[:b])
+        L = int(w.seq_lens[b])
+        wb = wl.Workload(name=f"{w.name}_r{b}", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                         num_blocks=w.num_blocks, layout=w.layout, q=w.q[q0:q1],
+                         key=w.key[kv0:kv0 + L], value=w.value[kv0:kv0 + L],
+                         slot_mapping=w.slot_mapping[kv0:kv0 + L], block_table=w.block_table[b:b + 1],
+                         seq_lens=w.seq_lens[b:b + 1],
+                         query_start_loc=torch.tensor([0, q1 - q0], dtype=torch.int32), scale=w.scale)
+        _prefill_vs_decode(wb, list(range(q1 - q0)))
+
+
+# ------------------------------------------------ schedule invariance ----
+
+def test_bounds_do_not_change_bits():
+    w = wl.decode()
+    dw, out, lse = _run(w)
+    for mq, ms in ((1, 8192), (3, 7168), (40, 20000), (300, 7200)):
+        o2, l2 = dw.attention(max_query_len=mq, max_seq_len=ms)
+        assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+        _bitwise(out, o2, f"decode bounds mq={mq} ms={ms} [{pagedattn.last_launch_info()}]")
+        _bitwise(lse, l2, "decode lse")
+
+
+def test_batch_composition_and_order_do_not_change_bits():
+    w = wl.decode()
+    dw, out, lse = _run(w)
+    perm = [2, 0, 3, 1]
+    dev = out.device
+    o2, l2 = dw.attention(q=dw.q[perm].contiguous(), block_tables=dw.block_tables[perm].contiguous(),
+                          seq_lens=dw.seq_lens[perm].contiguous())
+    _bitwise(out[perm], o2, "decode with requests permuted")
+    _bitwise(lse[perm], l2, "lse with requests permuted")
+    for b in range(4):
+        o1, l1 = dw.attention(q=dw.q[b:b + 1], block_tables=dw.block_tables[b:b + 1].contiguous(),
+                              seq_lens=dw.seq_lens[b:b + 1].contiguous(),
+                              query_start_loc=torch.tensor([0, 1], dtype=torch.int32, device=dev),
+                              max_seq_len=int(w.seq_lens[b]))
+        _bitwise(out[b:b + 1], o1, f"request {b} alone")
+        _bitwise(lse[b:b + 1], l1, f"request {b} alone (lse)")
+
+
+def test_prefill_bounds_and_schedule_switch():
+    """The same prefill rows through in-CTA and split-KV schedules (the
+    schedule follows host bounds only) stay bit-identical."""
+    w = wl.long_prefill(1024, pool_factor=3)
+    dw, out, lse = _run(w)
+    o2, l2 = dw.attention(max_query_len=4096, max_seq_len=65536)
+    _bitwise(out, o2, f"prefill larger bounds [{pagedattn.last_launch_info()}]")
+    _bitwise(lse, l2, "prefill larger bounds (lse)")
+
+
+# --------------------------------------------------------- edge cases ----
+
+def test_empty_and_zero_query_requests():
+    w = wl.decode(seq_lens=(513, 40, 16), num_blocks=128)
+    dw, out, lse = _run(w)
+    # an empty call launches nothing and succeeds
+    empty = torch.empty((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    pagedattn.paged_attention(empty, dw.k_cache, dw.v_cache, dw.block_tables, dw.seq_lens,
+                              torch.zeros(4, dtype=torch.int32, device="cuda"), w.scale, 0, 513)
+    # request 1 with zero new tokens: rows of the others are unchanged
+    qsl = torch.tensor([0, 1, 1, 2], dtype=torch.int32, device="cuda")
+    q2 = dw.q[[0, 2]].contiguous()
+    o2, l2 = dw.attention(q=q2, query_start_loc=qsl)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    _bitwise(out[[0, 2]], o2, "zero-length request in the batch")
+
+
+def test_single_token_sequence():
+    w = wl.decode(seq_lens=(1, 2, 17), num_blocks=64)
+    dw, out, lse = _run(w)
+    _compare(w, out, lse)
+    v0 = w.value[0].cuda()
+    for h in range(8):
+        assert torch.equal(out[0, h], v0[h // 4])
+
+
+# ------------------------------------------------------ invalid metadata ----
+
+def test_bad_block_id_flags_and_nans_only_that_request():
+    w = wl.decode()
+    dw, out, lse = _run(w)
+    bt = dw.block_tables.clone()
+    bt[1, 3] = w.num_blocks + 5
+    o2, l2 = dw.attention(block_tables=bt)
+    st, idx = pagedattn.check_errors()
+    assert st == pagedattn.PA_ERR_BAD_METADATA and idx == 1
+    assert torch.isnan(o2[1].float()).all() and torch.isnan(l2[1]).all()
+    keep = [0, 2, 3]
+    _bitwise(out[keep], o2[keep], "other requests after a bad block id")
+
+
+def test_seq_len_shorter_than_query_flags():
+    w = wl.decode(seq_lens=(513, 40, 16), num_blocks=128)
+    dw, out, lse = _run(w)
+    sl = dw.seq_lens.clone()
+    sl[2] = 0                          # one query token but no cached key
+    o2, l2 = dw.attention(seq_lens=sl)
+    st, idx = pagedattn.check_errors()
+    assert st == pagedattn.PA_ERR_BAD_METADATA and idx == 2
+    assert torch.isnan(o2[2].float()).all()
+    _bitwise(out[:2], o2[:2], "other requests after seq_len < q_len")
+
+
+def test_bound_violation_flags():
+    w = wl.decode(seq_lens=(513, 40, 16), num_blocks=128)
+    dw, out, lse = _run(w)
+    o2, l2 = dw.attention(max_seq_len=100)      # request 0 has 513 keys
+    st, idx = pagedattn.check_errors()
+    assert st == pagedattn.PA_ERR_BAD_METADATA and idx == 0
+    _bitwise(out[1:], o2[1:], "other requests after a bound violation")
