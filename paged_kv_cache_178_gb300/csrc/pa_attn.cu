@@ -1,31 +1,38 @@
 // K2: paged grouped-query attention for sm_103a (head dims 128 and 256).
 //
 // One CTA owns a 128-row tile of (query token, query head) rows of one
-// request and one KV head: rows r = t*G + hh are query token t of the tile
-// and query head kvh*G + hh, so the G heads sharing a KV head share every
-// K/V tile ("test(rocm): ReshapeAndCache->PagedAttention composition at real
-// dims", What changed: Hq=8, Hkv=2).  Roles (256 threads):
-//   warp 0     TMA producer: Q once, then per 128-key tile one 64-column box
-//              per 16-token page for K and for V, block ids read from the
-//              request's table; pages past the last needed key are not read
-//              ("fix(rocm): stabilize direct paged CK attention for bitwise
-//              R/R", Changes: tail-page padding and sanitising).
-//   warp 1     tcgen05 issuer: S = Q.K^T into TMEM (double buffered), then
-//              O += P.V into TMEM; zeroes V rows of keys past the last needed
-//              key so a masked probability never meets a poisoned value.
-//   warps 4-7  softmax / correction / epilogue, one thread per row.
+// request and one KV head: row r = t*G + hh is query token t of the tile and
+// query head kvh*G + hh, so the G heads sharing a KV head share every K/V
+// tile ("test(rocm): ReshapeAndCache->PagedAttention composition at real
+// dims", What changed: Hq=8, Hkv=2).  Roles (512 threads):
+//   warp 0       TMA producer: Q once, then per 128-key tile one 64-column box
+//                per 16-token page for K and for V, block ids read from the
+//                request's table (and range-checked) as it goes; pages past
+//                the last needed key are never read ("fix(rocm): stabilize
+//                direct paged CK attention for bitwise R/R", Changes: tail-page
+//                padding and sanitising).
+//   warp 1       tcgen05 issuer: S = Q.K^T into TMEM (two buffers), then
+//                O += P.V with P read from TMEM; zeroes V rows of keys past the
+//                last needed key so a zero probability never meets garbage.
+//   warps 4-11   softmax, two halves: warps 4-7 own score columns 0-63, warps
+//                8-11 columns 64-127, one TMEM lane (row) per thread.
+//   warps 12-15  correction: chunk folds, epilogue, split partial states.
 //
 // Fixed arithmetic (same page, intro and Changes: one schedule for every
-// shape, no implicit FMA contraction): every row follows the same sequence
+// shape, no implicit FMA contraction).  Every row follows the same sequence
 // of operations whatever the batch, query length, other rows or launch
 // bounds, so prefill and decode agree bit for bit:
 //   C1  KV tiles of 128 keys aligned to key 0; one MMA shape (M=128, K-steps
 //       of 16 in ascending order, BF16 in, FP32 accumulate).
-//   C2  s2 = S * (scale*log2 e) (one fp32 multiply, product formed on host).
+//   C2  s2 = S * (scale*log2 e) (one fp32 multiply; the product is formed once
+//       on the host).
 //   C3  lazy online softmax over a chunk's tiles: the reference max m moves
 //       only when a tile max exceeds m + 8 (then l and O are scaled by
 //       exp2(m_old - m_new)); p = exp2(s2 - m) for allowed keys, exactly 0
-//       otherwise; the tile's row sum is a fixed 8-way interleaved sum.
+//       otherwise.  Tile row sum: for each 64-column half an 8-way
+//       interleaved sum (accumulator k sums the half's columns k, k+8, ..,
+//       k+56 in order, then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))); tile sum =
+//       half0 + half1.
 //   C4  P rounded to BF16 (RNE) before P.V.
 //   C5  head dim 128: chunks of 256 keys aligned to key 0, each starting
 //       fresh; chunk states fold left to right with one fold function
@@ -34,6 +41,7 @@
 //   C6  out = O * rcp_rn(l) -> BF16 RNE; lse = (m + log2 l) * ln 2.
 #include <cuda_bf16.h>
 #include <cstdio>
+#include <cstring>
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -42,6 +50,7 @@ namespace pa {
 
 constexpr int kRows = 128;          // M of every MMA: rows per tile
 constexpr int kKeys = 128;          // keys per KV tile
+constexpr int kThreads = 512;
 constexpr float kTau = 8.0f;        // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -51,26 +60,33 @@ template <int DH>
 struct Cfg;
 template <>
 struct Cfg<128> {
-    static constexpr int kStages = 2;      // K/V smem stages
-    static constexpr int kPBufs = 2;       // P smem buffers
+    static constexpr int kStagesK = 3;     // K smem stages
+    static constexpr int kStagesV = 2;     // V smem stages
     static constexpr int kChunk = 256;     // keys per chunk (0 = one chunk)
     static constexpr int kOCol = 256;      // TMEM column of the chunk accumulator
     static constexpr int kAccCol = 384;    // TMEM column of the folded accumulator
 };
 template <>
 struct Cfg<256> {
-    static constexpr int kStages = 1;
-    static constexpr int kPBufs = 1;
+    static constexpr int kStagesK = 1;
+    static constexpr int kStagesV = 1;
     static constexpr int kChunk = 0;
     static constexpr int kOCol = 256;
     static constexpr int kAccCol = -1;
 };
 
+// Small shared arrays after the tiles: barriers, flags, the two per-row
+// exchange buffers of the softmax halves and the chunk (m, l) hand-off.
+constexpr int kSmallBytes = 512 /*barriers*/ + 64 /*flags*/ + 2 * 2 * kRows * 4 + 2 * kRows * 2 * 4;
+
+template <int DH>
+constexpr size_t tile_bytes() { return (size_t)(DH / 64) * 16384; }
+
 template <int DH>
 constexpr size_t smem_bytes()
 {
-    return 1024 /*align slack*/ + (size_t)(DH / 64) * 16384 * (1 + 2 * Cfg<DH>::kStages) +
-           (size_t)Cfg<DH>::kPBufs * 32768 + 256 /*barriers and flags*/;
+    return 1024 /*alignment slack*/ + tile_bytes<DH>() * (1 + Cfg<DH>::kStagesK + Cfg<DH>::kStagesV) +
+           kSmallBytes;
 }
 
 struct AttnParams {
@@ -138,30 +154,30 @@ __device__ __forceinline__ float lse_of(float m, float l)
     return __fmul_rn(__fadd_rn(m, __log2f(l)), kLn2);
 }
 
-// Bounded mbarrier wait.  Gives up when another thread of the CTA already
-// gave up (abort flag) or after kWaitLimitNs, latching PA_ERR_TIMEOUT.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                      ErrState *err)
+// Bounded mbarrier wait (inline: no call, so no register spills around it).
+// Gives up when another thread of the CTA already gave up (abort flag) or
+// after kWaitLimitNs, latching PA_ERR_TIMEOUT.
+// The first timeout records (block index << 8) | barrier slot as its index.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         ErrState *err, int where)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_timer_ns();
-    while (true) {
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity))
-                return true;
+    while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag)
             return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
-            record_error(err, kErrTimeout, -1);
+            record_error(err, kErrTimeout, ((long long)blockIdx.x << 8) | where);
             return false;
         }
     }
+    return true;
 }
 
-// Wait without the abort shortcut (used to drain in-flight work on exit).
-__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity)
+// Wait without the abort shortcut (drains in-flight work on exit).
+__device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -175,30 +191,47 @@ __device__ __forceinline__ void named_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ORs a predicate over the participating threads, so
+// every participant takes the same branch afterwards.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 q, %1, 0;\n\t"
+                 "bar.red.or.pred p, %2, %3, q;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+                 : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Store 32 consecutive output values (fp32, already normalised) as BF16.
-__device__ __forceinline__ void store_out32(__nv_bfloat16 *dst, const float (&v)[32])
+// Store 32 consecutive output values (fp32 bit patterns, already
+// normalised) as BF16.
+__device__ __forceinline__ void store_out32(__nv_bfloat16 *dst, const uint32_t (&v)[32])
 {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    for (int i = 0; i < 4; ++i) {
+        const float *f = reinterpret_cast<const float *>(v) + 8 * i;
+        d[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                          pack_bf16x2(f[6], f[7]));
+    }
 }
 
 template <int DH>
-__device__ void write_nan_rows(const AttnParams &p, int64_t tok_first, int ntok, int kvh, int tid,
-                               int nthreads)
+__device__ void write_nan_rows(const AttnParams &p, int64_t tok_first, int ntok, int kvh)
 {
     const __nv_bfloat16 qnan = __ushort_as_bfloat16(0x7FC0);
     const int G = p.group;
     const int64_t total = (int64_t)ntok * G * DH;
-    for (int64_t e = tid; e < total; e += nthreads) {
+    for (int64_t e = threadIdx.x; e < total; e += blockDim.x) {
         const int64_t row = e / DH;
         const int d = (int)(e % DH);
         const int64_t t = tok_first + row / G;
@@ -209,101 +242,296 @@ __device__ void write_nan_rows(const AttnParams &p, int64_t tok_first, int ntok,
     }
 }
 
-// Last-arriving CTA of a split (request, KV head, query tile) folds the
-// chunk partial states left to right and writes out / lse -- C5, C6.
-template <int DH>
-__device__ void merge_partials(const AttnParams &p, const float *part0, int64_t unit_stride,
-                               int nchunks, int rows_valid, int64_t tok_first, int kvh, int tid,
-                               int nthreads)
+// Split-KV partial-state record of one chunk (fp32): m[R], l[R] padded to a
+// multiple of 4 floats, then O[R][DH] row-major (unnormalised).
+__host__ __device__ constexpr int64_t part_header_floats(int R) { return (2 * R + 3) / 4 * 4; }
+__host__ __device__ constexpr int64_t part_record_floats(int R, int DH)
 {
-    const int R = p.ws_rows;
-    const int G = p.group;
-    for (int e = tid; e < rows_valid * DH; e += nthreads) {
-        const int d = e / rows_valid;
-        const int row = e % rows_valid;
-        float ma = -INFINITY, la = 0.f, oa = 0.f;
-        for (int c = 0; c < nchunks; ++c) {
-            const float *pc = part0 + (int64_t)c * unit_stride;
-            const float mc = __ldcg(pc + row);
-            const float lc = __ldcg(pc + R + row);
-            const float oc = __ldcg(pc + 2 * R + (int64_t)d * R + row);
-            const Fold f = fold_coef(ma, la, mc, lc);
-            oa = fold_elem(oa, oc, f);
-            ma = f.m;
-            la = f.l;
-        }
-        const int64_t t = tok_first + row / G;
-        const int h = kvh * G + row % G;
-        p.out[(t * p.hq + h) * DH + d] = __float2bfloat16_rn(__fmul_rn(oa, __frcp_rn(la)));
-        if (d == 0 && p.lse)
-            p.lse[t * p.hq + h] = lse_of(ma, la);
-    }
+    return part_header_floats(R) + (int64_t)R * DH;
 }
 
+// Arrival on the (request, KV head, query tile) counter; the last CTA to
+// arrive folds the chunk partial states left to right and writes out / lse
+// (C5, C6).  All threads of the CTA take part; `work` is shared memory the
+// pipeline no longer uses.  The fold is staged: a segment of records is
+// copied to shared memory in one pass, the per-row coefficient chain
+// (fold_coef) runs once per row, then every element applies fold_elem in
+// chunk order -- the same operations, in the same order, as the in-CTA fold.
 template <int DH>
-__device__ void arrive_and_maybe_merge(const AttnParams &p, int b, int kvh, int qt, int nchunks,
-                                       int rows_valid, int64_t tok_first, int r, int *flag_last)
+__device__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int nchunks, int rv,
+                                       int64_t tok_first, int kvh, float *work, int work_floats,
+                                       int *flag_last)
 {
-    __threadfence();
-    named_sync(1, 128);
-    const int64_t unit_q = ((int64_t)b * p.hkv + kvh) * p.qtiles + qt;
-    if (r == 0) {
+    const int tid = threadIdx.x, nth = blockDim.x;
+    if (tid == 0) {
         const uint32_t old = atomicAdd(p.ws_cnt + unit_q, 1u);
         const int last = (old == (uint32_t)(nchunks - 1));
         if (last)
             p.ws_cnt[unit_q] = 0u;  // leave the workspace ready for the next call
         *flag_last = last;
     }
-    named_sync(1, 128);
-    if (*flag_last) {
-        __threadfence();
-        const int64_t unit_stride = (int64_t)p.ws_rows * (DH + 2);
-        const float *part0 = p.ws_part + unit_q * p.nch * unit_stride;
-        merge_partials<DH>(p, part0, unit_stride, nchunks, rows_valid, tok_first, kvh, r, 128);
+    __syncthreads();
+    if (!*flag_last)
+        return;
+    __threadfence();
+    const int R = p.ws_rows;
+    const int64_t hdr = part_header_floats(R);
+    const int64_t ustride = part_record_floats(R, DH);
+    const float *part0 = p.ws_part + unit_q * p.nch * ustride;
+    const int run_f = (2 * rv + 3) / 4 * 4;
+    float *s_acc = work;                 // [rv][DH] running O
+    float *s_run = s_acc + rv * DH;      // [rv][2] running (m, l)
+    float *s_seg = s_run + run_f;
+    const int per_chunk = rv * (DH + 5) + 8;
+    const int seg = max(1, (work_floats - rv * DH - run_f) / per_chunk);
+    for (int e = tid; e < rv * DH; e += nth)
+        s_acc[e] = 0.f;
+    for (int r = tid; r < rv; r += nth) {
+        s_run[2 * r] = -INFINITY;
+        s_run[2 * r + 1] = 0.f;
+    }
+    for (int c0 = 0; c0 < nchunks; c0 += seg) {
+        const int cn = min(seg, nchunks - c0);
+        float *s_ml = s_seg;                             // [cn][rv][2]
+        float *s_o = s_ml + (2 * cn * rv + 3) / 4 * 4;   // [cn][rv][DH]
+        float *s_cf = s_o + cn * rv * DH;                // [cn][rv][2]
+        int *s_md = reinterpret_cast<int *>(s_cf + 2 * cn * rv);  // [cn][rv]
+        // (a) stage the segment's records
+        for (int i = tid; i < cn * rv * 2; i += nth) {
+            const int c = i / (2 * rv), k = i % (2 * rv);
+            const int which = k / rv, r = k % rv;
+            s_ml[(c * rv + r) * 2 + which] = __ldcg(part0 + (c0 + c) * ustride + which * R + r);
+        }
+        const int vec_per_chunk = rv * DH / 4;
+        for (int i = tid; i < cn * vec_per_chunk; i += nth) {
+            const int c = i / vec_per_chunk, k = i % vec_per_chunk;
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(part0 + (c0 + c) * ustride + hdr) + k);
+            reinterpret_cast<float4 *>(s_o + c * rv * DH)[k] = v;
+        }
+        __syncthreads();
+        // (b) per-row coefficient chains
+        for (int r = tid; r < rv; r += nth) {
+            float ma = s_run[2 * r], la = s_run[2 * r + 1];
+            for (int c = 0; c < cn; ++c) {
+                const Fold f = fold_coef(ma, la, s_ml[(c * rv + r) * 2], s_ml[(c * rv + r) * 2 + 1]);
+                s_cf[(c * rv + r) * 2] = f.sa;
+                s_cf[(c * rv + r) * 2 + 1] = f.sc;
+                s_md[c * rv + r] = f.mode;
+                ma = f.m;
+                la = f.l;
+            }
+            s_run[2 * r] = ma;
+            s_run[2 * r + 1] = la;
+        }
+        __syncthreads();
+        // (c) per-element folds, chunk order
+        for (int e = tid; e < rv * DH; e += nth) {
+            const int r = e / DH;
+            float oa = s_acc[e];
+            for (int c = 0; c < cn; ++c) {
+                Fold f;
+                f.sa = s_cf[(c * rv + r) * 2];
+                f.sc = s_cf[(c * rv + r) * 2 + 1];
+                f.mode = s_md[c * rv + r];
+                oa = fold_elem(oa, s_o[c * rv * DH + e], f);
+            }
+            s_acc[e] = oa;
+        }
+        __syncthreads();
+    }
+    // (d) epilogue
+    const int G = p.group;
+    for (int e = tid; e < rv * DH; e += nth) {
+        const int r = e / DH, d = e % DH;
+        const float ma = s_run[2 * r], la = s_run[2 * r + 1];
+        const int64_t t = tok_first + r / G;
+        const int h = kvh * G + r % G;
+        p.out[(t * p.hq + h) * DH + d] = __float2bfloat16_rn(__fmul_rn(s_acc[e], __frcp_rn(la)));
+        if (d == 0 && p.lse)
+            p.lse[t * p.hq + h] = lse_of(ma, la);
     }
 }
 
+// Request metadata as every CTA reads it.
+struct ReqMeta {
+    int qs, qn, L;
+    bool sane;  // the query-token range is usable (rows can be written)
+    bool ok;    // lengths are consistent with each other and with the bounds
+};
+
+__device__ __forceinline__ ReqMeta read_meta(const AttnParams &p, int b)
+{
+    ReqMeta m;
+    const int qs = __ldg(p.qsl + b), qe = __ldg(p.qsl + b + 1), L = __ldg(p.seq_lens + b);
+    m.qs = qs;
+    m.qn = qe - qs;
+    m.L = L;
+    m.sane = qs >= 0 && m.qn >= 0 && (int64_t)qe <= p.num_q_tokens;
+    m.ok = m.sane && L >= m.qn && (int64_t)L <= (int64_t)p.max_blocks * 16 && m.qn <= p.max_query_len &&
+           L <= p.max_seq_len;
+    return m;
+}
+
+// Number of chunks a query tile needs: keys [0, kend) with kend one past the
+// tile's last query position.
+__device__ __forceinline__ int tile_chunks(const ReqMeta &m, int qt, int tq, int chunk)
+{
+    const int kend = m.L - m.qn + min(m.qn, (qt + 1) * tq);
+    return (kend + chunk - 1) / chunk;
+}
+
+struct Unit {
+    int b, kvh, qt, c;
+    bool valid;  // false: this CTA has nothing to do
+};
+
+// Split-KV schedule: CTA i takes the i-th non-empty (request, KV head, query
+// tile, chunk) unit, so every CTA with work comes first in the grid.  A
+// request whose lengths are inconsistent gets one unit per (KV head, query
+// tile) that only writes NaN rows.  Uses all threads; scratch in `s_int`
+// (>= 34 ints).
+__device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int cnt = 0;
+    if (tid < p.num_seqs) {
+        const ReqMeta m = read_meta(p, tid);
+        if (!m.sane) {
+            if (blockIdx.x == 0)
+                record_error(p.err, kErrBadMetadata, tid);
+        } else {
+            const int qtl = (m.qn + p.tq - 1) / p.tq;
+            if (!m.ok) {
+                cnt = qtl;
+            } else {
+                for (int qt = 0; qt < qtl; ++qt)
+                    cnt += tile_chunks(m, qt, p.tq, chunk);
+            }
+            cnt *= p.hkv;
+        }
+    }
+    // block-wide exclusive prefix sum of cnt
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        s_int[warp] = incl;
+    if (tid == 0)
+        s_int[32] = -1;
+    __syncthreads();
+    int wpre = 0;
+    for (int w = 0; w < warp; ++w)
+        wpre += s_int[w];
+    const long long excl = (long long)wpre + incl - cnt;
+    const long long target = blockIdx.x;
+    if (cnt > 0 && target >= excl && target < excl + cnt) {
+        s_int[32] = tid;
+        s_int[33] = (int)(target - excl);
+    }
+    __syncthreads();
+    Unit u{0, 0, 0, 0, false};
+    const int b = s_int[32];
+    if (b < 0)
+        return u;
+    int r = s_int[33];
+    const ReqMeta m = read_meta(p, b);
+    const int qtl = (m.qn + p.tq - 1) / p.tq;
+    u.b = b;
+    u.valid = true;
+    if (!m.ok) {
+        u.kvh = r / qtl;
+        u.qt = r % qtl;
+        return u;
+    }
+    int per_kvh = 0;
+    for (int qt = 0; qt < qtl; ++qt)
+        per_kvh += tile_chunks(m, qt, p.tq, chunk);
+    u.kvh = r / per_kvh;
+    r %= per_kvh;
+    for (int qt = 0; qt < qtl; ++qt) {
+        const int n = tile_chunks(m, qt, p.tq, chunk);
+        if (r < n) {
+            u.qt = qt;
+            u.c = r;
+            break;
+        }
+        r -= n;
+    }
+    return u;
+}
+
 template <int DH>
-__global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ AttnParams p)
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = Cfg<DH>;
-    constexpr int NKB = DH / 64;            // 64-column (128-byte) blocks of the head dim
-    constexpr int TILE_BYTES = NKB * 16384;  // 128 rows (or keys) x DH BF16
-    constexpr int NST = C::kStages;
-    constexpr int NP = C::kPBufs;
+    constexpr int NKB = DH / 64;                     // 64-column (128-byte) blocks of the head dim
+    constexpr int TILE_BYTES = (int)tile_bytes<DH>();  // 128 rows (or keys) x DH BF16
+    constexpr int NSK = C::kStagesK;
+    constexpr int NSV = C::kStagesV;
     constexpr bool CHUNKED = C::kChunk > 0;
     constexpr int CHUNK_DIV = CHUNKED ? C::kChunk : 1;  // divisor used only when CHUNKED
+    constexpr int TPC = CHUNKED ? C::kChunk / kKeys : 1;  // tiles per chunk
     constexpr uint32_t ACC_COL = C::kAccCol < 0 ? 0u : (uint32_t)C::kAccCol;
     constexpr uint32_t ID_QK = idesc_bf16_f32(kRows, kKeys, false);
     constexpr uint32_t ID_PV = idesc_bf16_f32(kRows, DH, true);
     // barrier slots
-    constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_KE = B_VF + NST, B_VE = B_KE + NST;
-    constexpr int B_SF = B_VE + NST, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PV = B_PF + NP;
-    constexpr int B_OF = B_PV + NP, B_DONE = B_OF + 1, NBARS = B_DONE + 1;
-    static_assert(NBARS * 8 + 32 <= 256, "barrier area");
+    constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
+    constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_CR = B_PV + 2;
+    constexpr int B_OF = B_CR + 2, B_PROD = B_OF + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
+    static_assert(NBARS * 8 <= 512, "barrier area");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + TILE_BYTES;
+    uint8_t *sV = sK + NSK * TILE_BYTES;
+    uint8_t *small = sV + NSV * TILE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small);
+    int *sflags = reinterpret_cast<int *>(small + 512);  // [0] abort [1] tmem [2] last [3] bad
+    float *s_x = reinterpret_cast<float *>(small + 512 + 64);   // [2 exchanges][2 halves][128]
+    float *s_ml = s_x + 2 * 2 * kRows;                          // [2 chunk parities][128][2]
+    volatile int *abort_flag = sflags;
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    // bounded wait on barrier slot i for the given phase parity
+    auto wb = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, abort_flag, p.err, i); };
+    const int tid = threadIdx.x;
+    const int warp = tid / 32, lane = tid % 32;
+    float *const merge_work = reinterpret_cast<float *>(sK);
+    constexpr int kMergeWorkFloats = (NSK + NSV) * TILE_BYTES / 4;
 
     // ---------------------------------------------------------- work unit --
-    long long u = blockIdx.x;
-    const int c_grid = (int)(u % p.nch);
-    u /= p.nch;
-    const int qt = (int)(u % p.qtiles);
-    u /= p.qtiles;
-    const int kvh = (int)(u % p.hkv);
-    const int b = (int)(u / p.hkv);
-    const int tid = threadIdx.x;
-    if (b >= p.num_seqs)
-        return;
-    const int qs = p.qsl[b], qe = p.qsl[b + 1], L = p.seq_lens[b];
-    const int qn = qe - qs;
-    const bool rows_sane = qs >= 0 && qn >= 0 && (int64_t)qe <= p.num_q_tokens;
-    const bool meta_ok = rows_sane && L >= qn && (int64_t)L <= (int64_t)p.max_blocks * 16 &&
-                         qn <= p.max_query_len && L <= p.max_seq_len;
+    int b, kvh, qt, c_grid = 0;
+    if (p.split) {
+        const Unit un = split_unit(p, CHUNK_DIV, reinterpret_cast<int *>(s_x));
+        if (!un.valid)
+            return;
+        b = un.b;
+        kvh = un.kvh;
+        qt = un.qt;
+        c_grid = un.c;
+    } else {
+        // longest work first: later query tiles see more keys
+        const long long u = blockIdx.x;
+        const long long nbh = (long long)p.num_seqs * p.hkv;
+        qt = p.qtiles - 1 - (int)(u / nbh);
+        kvh = (int)((u % nbh) % p.hkv);
+        b = (int)((u % nbh) / p.hkv);
+    }
+    const ReqMeta meta = read_meta(p, b);
+    const int qs = meta.qs, qn = meta.qn, L = meta.L;
     const int tok0 = qt * p.tq;
-    if (!meta_ok) {
-        if (qt == 0 && c_grid == 0 && tid == 0)
+    if (!meta.ok) {
+        if (!p.split && qt == p.qtiles - 1 && tid == 0)
             record_error(p.err, kErrBadMetadata, b);
-        if (rows_sane && c_grid == 0 && tok0 < qn)
-            write_nan_rows<DH>(p, (int64_t)qs + tok0, min(p.tq, qn - tok0), kvh, tid, blockDim.x);
+        if (p.split && tid == 0)
+            record_error(p.err, kErrBadMetadata, b);
+        if (meta.sane && tok0 < qn)
+            write_nan_rows<DH>(p, (int64_t)qs + tok0, min(p.tq, qn - tok0), kvh);
         return;
     }
     if (tok0 >= qn)
@@ -315,91 +543,48 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
     const int nchunks = CHUNKED ? (kend + CHUNK_DIV - 1) / CHUNK_DIV : 1;
     int kbeg = 0, kstop = kend;
     if (p.split) {
-        if (c_grid >= nchunks)
-            return;
         kbeg = c_grid * CHUNK_DIV;
         kstop = min(kbeg + CHUNK_DIV, kend);
     }
     const int t_begin = kbeg / kKeys;
     const int t_end = (kstop + kKeys - 1) / kKeys;
     const int n_it = t_end - t_begin;
+    const int nck = CHUNKED ? (n_it + TPC - 1) / TPC : 1;  // chunks this CTA processes
     const int npages_need = (kend + 15) / 16;
     const int32_t *bt_row = p.block_tables + (int64_t)b * p.max_blocks;
-
-    // Every block id this CTA will use must be inside the pool.
-    int bad = 0;
-    {
-        const int pg_end = min(t_end * 8, npages_need);
-        for (int pg = t_begin * 8 + tid; pg < pg_end; pg += blockDim.x) {
-            const int id = bt_row[pg];
-            bad |= (id < 0 || (int64_t)id >= p.num_blocks);
-        }
-    }
-    bad = __syncthreads_or(bad);
-
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem;
-    uint8_t *sK = sQ + TILE_BYTES;
-    uint8_t *sV = sK + NST * TILE_BYTES;
-    uint8_t *sP = sV + NST * TILE_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sP + NP * 32768);
-    int *sflags = reinterpret_cast<int *>(bars + NBARS);  // [0] abort [1] tmem [2] last
-    volatile int *abort_flag = sflags;
-    auto bar = [&](int i) { return smem_addr(&bars[i]); };
-    const int warp = tid / 32, lane = tid % 32;
-    const int unit_stride_f = p.ws_rows * (DH + 2);
-
-    if (bad) {
-        if (tid == 0)
-            record_error(p.err, kErrBadMetadata, b);
-        if (!p.split) {
-            write_nan_rows<DH>(p, tok_first, ntok, kvh, tid, blockDim.x);
-            return;
-        }
-        if (warp < 4)
-            return;
-        const int r = tid - 128;
-        const int64_t unit_q = ((int64_t)b * p.hkv + kvh) * p.qtiles + qt;
-        float *part = p.ws_part + (unit_q * p.nch + c_grid) * unit_stride_f;
-        if (r < rows_valid) {
-            part[r] = 0.f;
-            part[p.ws_rows + r] = __int_as_float(0x7FC00000);
-            for (int d = 0; d < DH; ++d)
-                part[2 * p.ws_rows + d * p.ws_rows + r] = __int_as_float(0x7FC00000);
-        }
-        arrive_and_maybe_merge<DH>(p, b, kvh, qt, nchunks, rows_valid, tok_first, r, &sflags[2]);
-        return;
-    }
+    const int64_t unit_q = ((int64_t)b * p.hkv + kvh) * p.qtiles + qt;
+    const int64_t rec_floats = part_record_floats(p.ws_rows, DH);
+    const int64_t rec_hdr = part_header_floats(p.ws_rows);
 
     // -------------------------------------------------------------- setup --
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B_KF + s), 1);
-            mbar_init(bar(B_VF + s), 1);
             mbar_init(bar(B_KE + s), 1);
+        }
+        for (int s = 0; s < NSV; ++s) {
+            mbar_init(bar(B_VF + s), 1);
             mbar_init(bar(B_VE + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_SE + i), 4);
-        }
-        for (int i = 0; i < NP; ++i) {
-            mbar_init(bar(B_PF + i), 4);
+            mbar_init(bar(B_PF + i), 8);
             mbar_init(bar(B_PV + i), 1);
+            mbar_init(bar(B_CR + i), 8);
         }
         mbar_init(bar(B_OF), 4);
+        mbar_init(bar(B_PROD), 1);
         mbar_init(bar(B_DONE), 1);
         sflags[0] = 0;
+        sflags[3] = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(&sflags[1]), 512);
         tmem_relinquish();
     }
-    if (tid == 32 * 2) {
+    if (tid == 64) {
         prefetch_tensormap(&p.tm_q);
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_v);
@@ -411,72 +596,93 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
-        bool ok = true;
-        int last_k_use[NST], last_v_use[NST];
-        for (int s = 0; s < NST; ++s) last_k_use[s] = last_v_use[s] = -1;
-        if (lane == 0) {
-            // Q box: 64 columns x G heads x tq tokens per 64-column block
+        bool ok = true, any_bad = false;
+        int last_k_use[NSK], last_v_use[NSV];
+        for (int s = 0; s < NSK; ++s) last_k_use[s] = -1;
+        for (int s = 0; s < NSV; ++s) last_v_use[s] = -1;
+        if (lane == 0)  // Q box: 64 columns x G heads x tq tokens per 64-column block
             mbar_arrive_expect_tx(bar(B_Q), NKB * 128 * p.group * p.tq);
-            for (int kb = 0; kb < NKB; ++kb)
-                tma_load_3d(smem_addr(sQ + kb * 16384), &p.tm_q, bar(B_Q), kb * 64, kvh * p.group,
-                            (int)tok_first);
-        }
-        int id_next = (lane < 8 && t_begin * 8 + lane < npages_need) ? bt_row[t_begin * 8 + lane] : 0;
+        __syncwarp();
+        if (lane < NKB)
+            tma_load_3d(smem_addr(sQ + lane * 16384), &p.tm_q, bar(B_Q), lane * 64, kvh * p.group,
+                        (int)tok_first);
+        auto load_id = [&](int t) {
+            const int pg = t * 8 + lane;
+            return (lane < 8 && pg < npages_need) ? __ldg(bt_row + pg) : 0;
+        };
+        int id_next = load_id(t_begin);
         for (int it = 0; ok && it < n_it; ++it) {
             const int t = t_begin + it;
-            const int id_cur = id_next;
-            id_next = (it + 1 < n_it && lane < 8 && (t + 1) * 8 + lane < npages_need)
-                          ? bt_row[(t + 1) * 8 + lane]
-                          : 0;
-            const int s = it % NST, use = it / NST;
+            int id = id_next;
+            if (it + 1 < n_it)
+                id_next = load_id(t + 1);
             const int np = min(8, npages_need - t * 8);
-            int ids[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ids[i] = __shfl_sync(0xffffffffu, id_cur, i);
+            const bool badl = lane < np && (id < 0 || (int64_t)id >= p.num_blocks);
+            if (badl)
+                id = 0;  // keep the pipeline flowing; the rows become NaN
+            any_bad |= __any_sync(0xffffffffu, badl);
+            const int my_page = lane / NKB, my_kb = lane % NKB;
+            const int my_id = __shfl_sync(0xffffffffu, id, my_page & 7);
+            const bool issue = lane < np * NKB;
+            // K
+            const int sk = it % NSK, uk = it / NSK;
             if (lane == 0) {
-                if (use >= 1)
-                    ok = wait_bar(bar(B_KE + s), (use - 1) & 1, abort_flag, p.err);
-                if (ok) {
-                    mbar_arrive_expect_tx(bar(B_KF + s), np * NKB * 2048);
-                    for (int i = 0; i < np; ++i)
-                        for (int kb = 0; kb < NKB; ++kb)
-                            tma_load_4d(smem_addr(sK + s * TILE_BYTES + kb * 16384 + i * 2048), &p.tm_k,
-                                        bar(B_KF + s), kb * 64, kvh, 0, ids[i]);
-                    last_k_use[s] = use;
-                }
-                if (ok && use >= 1)
-                    ok = wait_bar(bar(B_VE + s), (use - 1) & 1, abort_flag, p.err);
-                if (ok) {
-                    mbar_arrive_expect_tx(bar(B_VF + s), np * NKB * 2048);
-                    for (int i = 0; i < np; ++i)
-                        for (int kb = 0; kb < NKB; ++kb)
-                            tma_load_4d(smem_addr(sV + s * TILE_BYTES + kb * 16384 + i * 2048), &p.tm_v,
-                                        bar(B_VF + s), kb * 64, kvh, 0, ids[i]);
-                    last_v_use[s] = use;
-                }
+                if (uk >= 1)
+                    ok = wb(B_KE + sk, (uk - 1) & 1);
+                if (ok)
+                    mbar_arrive_expect_tx(bar(B_KF + sk), np * NKB * 2048);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        if (!ok && lane == 0) {
-            // Let issued copies land before the CTA's shared memory goes away.
-            for (int s = 0; s < NST; ++s) {
-                if (last_k_use[s] >= 0)
-                    wait_bar_drain(bar(B_KF + s), last_k_use[s] & 1);
-                if (last_v_use[s] >= 0)
-                    wait_bar_drain(bar(B_VF + s), last_v_use[s] & 1);
+            if (!ok)
+                break;
+            if (issue)
+                tma_load_4d(smem_addr(sK + sk * TILE_BYTES + my_kb * 16384 + my_page * 2048), &p.tm_k,
+                            bar(B_KF + sk), my_kb * 64, kvh, 0, my_id);
+            last_k_use[sk] = uk;
+            // V
+            const int sv = it % NSV, uv = it / NSV;
+            if (lane == 0) {
+                if (uv >= 1)
+                    ok = wb(B_VE + sv, (uv - 1) & 1);
+                if (ok)
+                    mbar_arrive_expect_tx(bar(B_VF + sv), np * NKB * 2048);
             }
-            wait_bar_drain(bar(B_Q), 0);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            if (issue)
+                tma_load_4d(smem_addr(sV + sv * TILE_BYTES + my_kb * 16384 + my_page * 2048), &p.tm_v,
+                            bar(B_VF + sv), my_kb * 64, kvh, 0, my_id);
+            last_v_use[sv] = uv;
         }
+        if (lane == 0) {
+            if (any_bad) {
+                record_error(p.err, kErrBadMetadata, b);
+                sflags[3] = 1;
+            }
+            mbar_arrive(bar(B_PROD));
+            if (!ok) {
+                // let issued copies land before the CTA's shared memory goes away
+                for (int s = 0; s < NSK; ++s)
+                    if (last_k_use[s] >= 0)
+                        wait_bar_drain(bar(B_KF + s), last_k_use[s] & 1);
+                for (int s = 0; s < NSV; ++s)
+                    if (last_v_use[s] >= 0)
+                        wait_bar_drain(bar(B_VF + s), last_v_use[s] & 1);
+                wait_bar_drain(bar(B_Q), 0);
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer --
         bool ok = true;
         if (lane == 0)
-            ok = wait_bar(bar(B_Q), 0, abort_flag, p.err);
+            ok = wb(B_Q, 0);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         auto issue_pv = [&](int j) -> bool {
-            const int s = j % NST;
+            const int sv = j % NSV;
             const int t = t_begin + j;
-            bool okj = wait_bar(bar(B_VF + s), (j / NST) & 1, abort_flag, p.err);
+            bool okj = wb(B_VF + sv, (j / NSV) & 1);
             okj = __all_sync(0xffffffffu, okj);
             if (!okj)
                 return false;
@@ -484,7 +690,7 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
                 // keys >= kend: zero their V rows (stale or poisoned data)
                 const int row0 = kend - t * kKeys;
                 const int nz = (kKeys - row0) * NKB * 8;
-                uint8_t *vs = sV + s * TILE_BYTES;
+                uint8_t *vs = sV + sv * TILE_BYTES;
                 for (int idx = lane; idx < nz; idx += 32) {
                     const int row = row0 + idx / (NKB * 8);
                     const int rem = idx % (NKB * 8);
@@ -495,45 +701,47 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
             }
             __syncwarp();
             if (lane == 0) {
-                okj = wait_bar(bar(B_PF + j % NP), (j / NP) & 1, abort_flag, p.err);
+                okj = wb(B_PF + (j & 1), (j >> 1) & 1);
                 const bool chunk_first = CHUNKED ? ((t * kKeys) % CHUNK_DIV == 0) : (j == 0);
                 const int k = CHUNKED ? (t * kKeys - kbeg) / CHUNK_DIV : 0;
                 if (okj && chunk_first && k > 0)
-                    okj = wait_bar(bar(B_OF), (k - 1) & 1, abort_flag, p.err);
+                    okj = wb(B_OF, (k - 1) & 1);
                 if (okj) {
                     tc_fence_after();
-                    const uint32_t pbase = smem_addr(sP + (j % NP) * 32768);
-                    const uint32_t vbase = smem_addr(sV + s * TILE_BYTES);
+                    // P of keys 0-63 sits in columns 0-31 of the S buffer, keys
+                    // 64-127 in columns 64-95 (each softmax half writes its own)
+                    const uint32_t pcol = tmem + (uint32_t)(j & 1) * kKeys;
+                    const uint32_t vbase = smem_addr(sV + sv * TILE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(pbase + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(vbase + kk * 2048, 16384, 1024);
-                        mma_bf16_ss(tmem + C::kOCol, a, bd, ID_PV, (kk > 0 || !chunk_first) ? 1u : 0u);
+                        const uint32_t acol = pcol + (kk / 4) * 64 + (kk % 4) * 8;
+                        mma_bf16_ts(tmem + C::kOCol, acol, bd, ID_PV, (kk > 0 || !chunk_first) ? 1u : 0u);
                     }
-                    mma_commit(bar(B_VE + s));
-                    mma_commit(bar(B_PV + j % NP));
+                    mma_commit(bar(B_VE + sv));
+                    mma_commit(bar(B_PV + (j & 1)));
                 }
             }
             return __shfl_sync(0xffffffffu, okj, 0);
         };
         for (int it = 0; ok && it <= n_it; ++it) {
             if (it < n_it) {
-                const int s = it % NST;
+                const int sk = it % NSK;
                 if (lane == 0) {
-                    ok = wait_bar(bar(B_KF + s), (it / NST) & 1, abort_flag, p.err);
-                    if (ok && it >= 2)
-                        ok = wait_bar(bar(B_SE + (it & 1)), ((it >> 1) - 1) & 1, abort_flag, p.err);
+                    // S buffer it&1 was last read (as P) by PV(it-2), issued earlier
+                    // from this thread, and tcgen05 MMAs from one thread run in order.
+                    ok = wb(B_KF + sk, (it / NSK) & 1);
                     if (ok) {
                         tc_fence_after();
                         const uint32_t qbase = smem_addr(sQ);
-                        const uint32_t kbase = smem_addr(sK + s * TILE_BYTES);
+                        const uint32_t kbase = smem_addr(sK + sk * TILE_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < DH / 16; ++kk) {
                             const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                            mma_bf16_ss(tmem + (it & 1) * kKeys, sdesc_sw128(qbase + off, 16, 1024),
+                            mma_bf16_ss(tmem + (uint32_t)(it & 1) * kKeys, sdesc_sw128(qbase + off, 16, 1024),
                                         sdesc_sw128(kbase + off, 16, 1024), ID_QK, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(B_KE + s));
+                        mma_commit(bar(B_KE + sk));
                         mma_commit(bar(B_SF + (it & 1)));
                     }
                 }
@@ -548,131 +756,170 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
             wait_bar_drain(bar(B_DONE), 0);
         }
         __syncwarp();
-    } else if (warp >= 4) {
-        // ------------------------------------------ softmax / epilogue WG --
-        const int r = tid - 128;
-        const int wq = warp - 4;
-        const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
+    } else if (warp >= 4 && warp < 12) {
+        // --------------------------------------------- softmax (2 halves) --
+        const int h = (warp - 4) / 4;       // column half
+        const int q4 = warp % 4;            // TMEM lane quadrant
+        const int r = q4 * 32 + lane;       // row
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const bool row_valid = r < rows_valid;
-        const bool warp_active = 32 * wq < rows_valid;
-        const int G = p.group;
-        const int pos = L - qn + tok0 + r / G;
-        const int64_t tok = tok_first + r / G;
-        const int head = kvh * G + r % G;
-        float m = -INFINITY, l = 0.f, m_acc = -INFINITY, l_acc = 0.f;
-        int nfold = 0;
-        bool ok = true;
-        for (int it = 0; ok && it < n_it; ++it) {
+        const bool warp_active = 32 * q4 < rows_valid;
+        const int pos = L - qn + tok0 + r / p.group;
+        float *xmax = s_x;                  // [2][128]
+        float *xsum = s_x + 2 * kRows;      // [2][128]
+        float m = -INFINITY, l = 0.f;
+        bool failed = false;  // a wait gave up: leave the loop together with the other half
+        for (int it = 0; it < n_it; ++it) {
             const int t = t_begin + it;
-            const int sb = it & 1, pb = it % NP;
-            ok = wait_bar(bar(B_SF + sb), (it >> 1) & 1, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const int sb = it & 1;
+            bool okw = !failed && wb(B_SF + sb, (it >> 1) & 1);
+            okw = __all_sync(0xffffffffu, okw);
             tc_fence_after();
-            float s[kKeys];
-            if (warp_active) {
-                uint32_t v[32];
+            const int nallow = row_valid ? max(0, min(64, pos - t * kKeys - 64 * h + 1)) : 0;
+            const uint32_t scol = tmem + lane_off + sb * kKeys + 64 * h;  // this half's S columns
+            // pass 1: tile max over allowed keys of this half
+            float pmax = -INFINITY;
+            if (warp_active && okw) {
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    tmem_ld32(tmem + lane_off + sb * kKeys + g4 * 32, v);
+                for (int g2 = 0; g2 < 2; ++g2) {
+                    uint32_t v[32];
+                    tmem_ld32(scol + g2 * 32, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[g4 * 32 + i] = __uint_as_float(v[i]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(B_SE + sb));
-            float m_new = m, corr = 1.f, tsum = 0.f;
-            bool need = false;
-            if (warp_active) {
-                const int nallow = row_valid ? max(0, min(kKeys, pos - t * kKeys + 1)) : 0;
-                float tmax = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    s[c] = __fmul_rn(s[c], p.scale_log2);
-                    tmax = (c < nallow) ? fmaxf(tmax, s[c]) : tmax;
-                }
-                if (tmax != -INFINITY) {
-                    if (m == -INFINITY) {
-                        m_new = tmax;
-                    } else if (tmax > __fadd_rn(m, kTau)) {
-                        m_new = tmax;
-                        corr = ex2(__fsub_rn(m, m_new));
-                        need = true;
+                    for (int i = 0; i < 32; ++i) {
+                        const float s2 = __fmul_rn(__uint_as_float(v[i]), p.scale_log2);
+                        pmax = (g2 * 32 + i < nallow) ? fmaxf(pmax, s2) : pmax;
                     }
                 }
-                float acc8[8];
-#pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    const float e = (c < nallow) ? ex2(__fsub_rn(s[c], m_new)) : 0.f;
-                    s[c] = e;
-                    if (c < 8)
-                        acc8[c] = e;
-                    else
-                        acc8[c & 7] = __fadd_rn(acc8[c & 7], e);
+            }
+            xmax[h * kRows + r] = pmax;
+            if (named_sync_or(1, 256, !okw)) {
+                failed = true;
+                break;
+            }
+            const float tmax = fmaxf(xmax[r], xmax[kRows + r]);
+            float m_new = m, corr = 1.f;
+            bool need = false;
+            if (tmax != -INFINITY) {
+                if (m == -INFINITY) {
+                    m_new = tmax;
+                } else if (tmax > __fadd_rn(m, kTau)) {
+                    m_new = tmax;
+                    corr = ex2(__fsub_rn(m, m_new));
+                    need = true;
                 }
-                tsum = __fadd_rn(__fadd_rn(__fadd_rn(acc8[0], acc8[1]), __fadd_rn(acc8[2], acc8[3])),
-                                 __fadd_rn(__fadd_rn(acc8[4], acc8[5]), __fadd_rn(acc8[6], acc8[7])));
             }
-            // P buffer pb is free once PV(it - NP) has completed
-            if (it >= NP) {
-                ok = wait_bar(bar(B_PV + pb), ((it / NP) - 1) & 1, abort_flag, p.err);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            }
+            // pass 2: p = exp2(s2 - m), the half's fixed-order sum, P as BF16
+            float hs = 0.f;
             if (warp_active) {
-                uint8_t *prow = sP + pb * 32768 + r * 128;
+                float a[8];
+                uint32_t w[32];
 #pragma unroll
-                for (int c8 = 0; c8 < kKeys / 8; ++c8) {
-                    const int kb = c8 / 8, ch = c8 % 8;
-                    const uint4 w = make_uint4(pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]),
-                                               pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]),
-                                               pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]),
-                                               pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]));
-                    *reinterpret_cast<uint4 *>(prow + kb * 16384 + ((ch ^ (r & 7)) << 4)) = w;
+                for (int g2 = 0; g2 < 2; ++g2) {
+                    uint32_t v[32];
+                    tmem_ld32(scol + g2 * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const int c = g2 * 32 + i;
+                        const float s0 = __fmul_rn(__uint_as_float(v[i]), p.scale_log2);
+                        const float s1 = __fmul_rn(__uint_as_float(v[i + 1]), p.scale_log2);
+                        const float e0 = (c < nallow) ? ex2(__fsub_rn(s0, m_new)) : 0.f;
+                        const float e1 = (c + 1 < nallow) ? ex2(__fsub_rn(s1, m_new)) : 0.f;
+                        if (c < 8) {
+                            a[c & 7] = e0;
+                            a[(c + 1) & 7] = e1;
+                        } else {
+                            a[c & 7] = __fadd_rn(a[c & 7], e0);
+                            a[(c + 1) & 7] = __fadd_rn(a[(c + 1) & 7], e1);
+                        }
+                        w[c / 2] = pack_bf16x2(e0, e1);
+                    }
                 }
-                fence_proxy_async_smem();
+                hs = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
+                               __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
+                // P (BF16, two keys per column) overwrites this half's first 32 S
+                // columns, after both S loads above completed
+                tmem_st32(scol, w);
             }
+            xsum[h * kRows + r] = hs;
+            named_sync(1, 256);
+            const float tsum = __fadd_rn(xsum[r], xsum[kRows + r]);
+            bool okr = true;
             if (__any_sync(0xffffffffu, need)) {
                 // O of this chunk must hold PV(it - 1) before it is rescaled
-                ok = wait_bar(bar(B_PV + (it - 1) % NP), ((it - 1) / NP) & 1, abort_flag, p.err);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                okr = __all_sync(0xffffffffu, wb(B_PV + ((it - 1) & 1), ((it - 1) >> 1) & 1));
+                failed = !okr;
+            }
+            if (__any_sync(0xffffffffu, need) && okr) {
                 tc_fence_after();
                 const float f = need ? corr : 1.f;
 #pragma unroll 1
-                for (int g = 0; g < DH / 32; ++g) {
+                for (int g = 0; g < DH / 64; ++g) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + C::kOCol + g * 32, v);
+                    const uint32_t col = tmem + lane_off + C::kOCol + (DH / 2) * h + g * 32;
+                    tmem_ld32(col, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fmul_rn(__uint_as_float(v[i]), f));
-                    tmem_st32(tmem + lane_off + C::kOCol + g * 32, v);
+                    tmem_st32(col, v);
                 }
-                tmem_wait_st();
+            }
+            tmem_wait_st();
+            l = need ? __fadd_rn(__fmul_rn(l, corr), tsum) : __fadd_rn(l, tsum);
+            m = m_new;
+            const bool chunk_end = (it == n_it - 1) || (CHUNKED && ((t + 1) * kKeys) % CHUNK_DIV == 0);
+            const int k = CHUNKED ? it / TPC : 0;
+            if (chunk_end && h == 0) {
+                s_ml[((k & 1) * kRows + r) * 2] = m;
+                s_ml[((k & 1) * kRows + r) * 2 + 1] = l;
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(B_PF + pb));
-            l = need ? __fadd_rn(__fmul_rn(l, corr), tsum) : __fadd_rn(l, tsum);
-            m = m_new;
-
-            const bool final_tile = (it == n_it - 1);
-            const bool chunk_end = final_tile || (CHUNKED && ((t + 1) * kKeys) % CHUNK_DIV == 0);
-            if (!chunk_end)
-                continue;
-            ok = wait_bar(bar(B_PV + pb), (it / NP) & 1, abort_flag, p.err);
+            if (lane == 0) {
+                mbar_arrive(bar(B_PF + sb));
+                if (chunk_end)
+                    mbar_arrive(bar(B_CR + (k & 1)));
+            }
+            if (chunk_end) {
+                m = -INFINITY;
+                l = 0.f;
+            }
+        }
+    } else if (warp >= 12) {
+        // ----------------------------------------------------- correction --
+        const int q4 = warp % 4;
+        const int r = q4 * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const bool row_valid = r < rows_valid;
+        const int G = p.group;
+        const int64_t tok = tok_first + r / G;
+        const int head = kvh * G + r % G;
+        float m_acc = -INFINITY, l_acc = 0.f;
+        int nfold = 0;  // chunks folded into the accumulator so far (CTA-uniform)
+        bool ok = true;
+        for (int k = 0; ok && k < nck; ++k) {
+            const int it_last = CHUNKED ? min((k + 1) * TPC, n_it) - 1 : n_it - 1;
+            const bool final_chunk = (k == nck - 1);
+            ok = wb(B_CR + (k & 1), (k >> 1) & 1);
+            if (ok)
+                ok = wb(B_PV + (it_last & 1), (it_last >> 1) & 1);
+            if (ok && final_chunk)
+                ok = wb(B_PROD, 0);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
+            const float m = s_ml[((k & 1) * kRows + r) * 2];
+            const float l = s_ml[((k & 1) * kRows + r) * 2 + 1];
+            const bool bad = final_chunk && sflags[3] != 0;
             if (p.split) {
-                // partial state of this CTA's chunk
-                const int64_t unit_q = ((int64_t)b * p.hkv + kvh) * p.qtiles + qt;
-                float *part = p.ws_part + (unit_q * p.nch + c_grid) * unit_stride_f;
-                const int R = p.ws_rows;
+                // partial state of this CTA's chunk: m, l and the O row
+                float *part = p.ws_part + (unit_q * p.nch + c_grid) * rec_floats;
+                const float qnan = __int_as_float(0x7FC00000);
                 if (row_valid) {
-                    part[r] = m;
-                    part[R + r] = l;
+                    part[r] = bad ? 0.f : m;
+                    part[p.ws_rows + r] = bad ? qnan : l;
                 }
+                float4 *orow = reinterpret_cast<float4 *>(part + rec_hdr + (int64_t)r * DH);
 #pragma unroll 1
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t v[32];
@@ -680,45 +927,51 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
                     tmem_wait_ld();
                     if (row_valid) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            __stcg(part + 2 * R + (int64_t)(g * 32 + i) * R + r, __uint_as_float(v[i]));
+                        for (int i = 0; i < 8; ++i)
+                            __stcg(orow + g * 8 + i,
+                                   bad ? make_float4(qnan, qnan, qnan, qnan)
+                                       : make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
                     }
                 }
-            } else if (final_tile) {
+                __threadfence();
+            } else if (final_chunk) {
                 // epilogue: out = fold(acc, chunk) / l
-                const Fold f = (nfold == 0) ? fold_coef(-INFINITY, 0.f, m, l) : fold_coef(m_acc, l_acc, m, l);
+                const Fold f = fold_coef(m_acc, l_acc, m, l);
                 const float inv = __frcp_rn(f.l);
+                const bool acc_live = nfold > 0;  // uniform: tcgen05.ld is warp-collective
 #pragma unroll 1
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t vc[32], va[32];
                     tmem_ld32(tmem + lane_off + C::kOCol + g * 32, vc);
-                    if (nfold > 0)
+                    if (acc_live)
                         tmem_ld32(tmem + lane_off + ACC_COL + g * 32, va);
                     tmem_wait_ld();
-                    float o[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float oa = (nfold > 0) ? __uint_as_float(va[i]) : 0.f;
-                        o[i] = __fmul_rn(fold_elem(oa, __uint_as_float(vc[i]), f), inv);
+                        const float oa = acc_live ? __uint_as_float(va[i]) : 0.f;
+                        vc[i] = bad ? 0x7FC00000u
+                                    : __float_as_uint(__fmul_rn(fold_elem(oa, __uint_as_float(vc[i]), f), inv));
                     }
                     if (row_valid)
-                        store_out32(p.out + (tok * p.hq + head) * DH + g * 32, o);
+                        store_out32(p.out + (tok * p.hq + head) * DH + g * 32, vc);
                 }
                 if (row_valid && p.lse)
-                    p.lse[tok * p.hq + head] = lse_of(f.m, f.l);
+                    p.lse[tok * p.hq + head] = bad ? __int_as_float(0x7FC00000) : lse_of(f.m, f.l);
             } else {
                 // fold this chunk into the running accumulator (TMEM)
-                const Fold f = (nfold == 0) ? fold_coef(-INFINITY, 0.f, m, l) : fold_coef(m_acc, l_acc, m, l);
+                const Fold f = fold_coef(m_acc, l_acc, m, l);
+                const bool acc_live = nfold > 0;  // uniform: tcgen05.ld is warp-collective
 #pragma unroll 1
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t vc[32], va[32];
                     tmem_ld32(tmem + lane_off + C::kOCol + g * 32, vc);
-                    if (nfold > 0)
+                    if (acc_live)
                         tmem_ld32(tmem + lane_off + ACC_COL + g * 32, va);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float oa = (nfold > 0) ? __uint_as_float(va[i]) : 0.f;
+                        const float oa = acc_live ? __uint_as_float(va[i]) : 0.f;
                         va[i] = __float_as_uint(fold_elem(oa, __uint_as_float(vc[i]), f));
                     }
                     tmem_st32(tmem + lane_off + ACC_COL + g * 32, va);
@@ -730,13 +983,9 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
             }
             tc_fence_before();
             __syncwarp();
-            if (!final_tile && lane == 0)
+            if (!final_chunk && lane == 0)
                 mbar_arrive(bar(B_OF));
-            m = -INFINITY;
-            l = 0.f;
         }
-        if (p.split && ok)
-            arrive_and_maybe_merge<DH>(p, b, kvh, qt, nchunks, rows_valid, tok_first, r, &sflags[2]);
     }
 
     tc_fence_before();
@@ -745,6 +994,9 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (p.split)
+        split_arrive_and_merge<DH>(p, unit_q, nchunks, rows_valid, tok_first, kvh, merge_work,
+                                   kMergeWorkFloats, &sflags[2]);
 }
 
 // ------------------------------------------------------------------ host --
@@ -775,7 +1027,7 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     if (pl.split) {
         const size_t units_q = (size_t)full_ctas;
         pl.ws_counter_bytes = ((units_q * 4 + 255) / 256) * 256;
-        pl.ws_bytes = pl.ws_counter_bytes + units_q * pl.nch * (size_t)pl.ws_rows * (head_dim + 2) * 4;
+        pl.ws_bytes = pl.ws_counter_bytes + units_q * pl.nch * (size_t)part_record_floats(pl.ws_rows, head_dim) * 4;
     }
     pl.grid = full_ctas * pl.nch;
     *plan = pl;
@@ -843,7 +1095,7 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.split = pl.split ? 1 : 0;
     // C2: scale * log2(e) formed once, in fp32, on the host
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    attn_kernel<DH><<<(unsigned)pl.grid, 256, smem_bytes<DH>(), stream>>>(p);
+    attn_kernel<DH><<<(unsigned)pl.grid, kThreads, smem_bytes<DH>(), stream>>>(p);
     return cudaGetLastError();
 }
 
