@@ -155,7 +155,7 @@ PA_API size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_
  *                       maximum query length; KV scheduling bound in the graph
  *                       identity).  A request exceeding them latches
  *                       PA_ERR_BAD_METADATA.
- *   scale             : softmax scale (typically 1/sqrt(Dh)).
+ *   scale             : softmax scale, finite and > 0 (typically 1/sqrt(Dh)).
  *   workspace         : device scratch of at least
  *                       pa_paged_attention_workspace_size(...) bytes, 256-byte
  *                       aligned, zero-filled before its first use; the library

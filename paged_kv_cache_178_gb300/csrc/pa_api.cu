@@ -216,7 +216,7 @@ pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_
         return PA_ERR_INVALID_ARG;
     if (num_q_heads % cache->num_kv_heads != 0 || num_q_heads / cache->num_kv_heads > 128)
         return PA_ERR_UNSUPPORTED;
-    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    if (!(scale > 0.f) || scale == INFINITY)  // also rejects NaN
         return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || num_q_tokens == 0 || max_query_len == 0) {
         snprintf(g_last_info, sizeof g_last_info, "attention: empty batch (nothing launched)");

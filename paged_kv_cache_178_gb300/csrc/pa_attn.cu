@@ -24,12 +24,13 @@
 // bounds, so prefill and decode agree bit for bit:
 //   C1  KV tiles of 128 keys aligned to key 0; one MMA shape (M=128, K-steps
 //       of 16 in ascending order, BF16 in, FP32 accumulate).
-//   C2  s2 = S * (scale*log2 e) (one fp32 multiply; the product is formed once
-//       on the host).
+//   C2  c = scale*log2 e is formed once, in fp32, on the host (scale > 0).
+//       Tile max in log2 units: (max of the raw scores S over allowed keys)
+//       * c, one fp32 multiply.
 //   C3  lazy online softmax over a chunk's tiles: the reference max m moves
 //       only when a tile max exceeds m + 8 (then l and O are scaled by
-//       exp2(m_old - m_new)); p = exp2(s2 - m) for allowed keys, exactly 0
-//       otherwise.  Tile row sum: for each 64-column half an 8-way
+//       exp2(m_old - m_new)); p = exp2(fma(S, c, -m)) for allowed keys,
+//       exactly 0 otherwise.  Tile row sum: for each 64-column half an 8-way
 //       interleaved sum (accumulator k sums the half's columns k, k+8, ..,
 //       k+56 in order, then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))); tile sum =
 //       half0 + half1.
@@ -281,9 +282,10 @@ __device__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int 
     const int run_f = (2 * rv + 3) / 4 * 4;
     float *s_acc = work;                 // [rv][DH] running O
     float *s_run = s_acc + rv * DH;      // [rv][2] running (m, l)
-    float *s_seg = s_run + run_f;
+    float *s_run2 = s_run + run_f;       // [rv][2] (m, l) after the current segment
+    float *s_seg = s_run2 + run_f;
     const int per_chunk = rv * (DH + 5) + 8;
-    const int seg = max(1, (work_floats - rv * DH - run_f) / per_chunk);
+    const int seg = max(1, (work_floats - rv * DH - 2 * run_f) / per_chunk);
     for (int e = tid; e < rv * DH; e += nth)
         s_acc[e] = 0.f;
     for (int r = tid; r < rv; r += nth) {
@@ -296,46 +298,74 @@ __device__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int 
         float *s_o = s_ml + (2 * cn * rv + 3) / 4 * 4;   // [cn][rv][DH]
         float *s_cf = s_o + cn * rv * DH;                // [cn][rv][2]
         int *s_md = reinterpret_cast<int *>(s_cf + 2 * cn * rv);  // [cn][rv]
-        // (a) stage the segment's records
+        // (a) stage the segment's records: every copy in flight at once
         for (int i = tid; i < cn * rv * 2; i += nth) {
             const int c = i / (2 * rv), k = i % (2 * rv);
             const int which = k / rv, r = k % rv;
-            s_ml[(c * rv + r) * 2 + which] = __ldcg(part0 + (c0 + c) * ustride + which * R + r);
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(s_ml + (c * rv + r) * 2 + which)),
+                         "l"(part0 + (c0 + c) * ustride + which * R + r)
+                         : "memory");
         }
         const int vec_per_chunk = rv * DH / 4;
         for (int i = tid; i < cn * vec_per_chunk; i += nth) {
             const int c = i / vec_per_chunk, k = i % vec_per_chunk;
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(part0 + (c0 + c) * ustride + hdr) + k);
-            reinterpret_cast<float4 *>(s_o + c * rv * DH)[k] = v;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(s_o + c * rv * DH + 4 * k)),
+                         "l"(part0 + (c0 + c) * ustride + hdr + 4 * k)
+                         : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+        // (b) fold coefficients of every (row, chunk).  The running max before
+        //     chunk c is the max over the earlier chunks (fmaxf is exact and
+        //     a chunk without keys holds -inf), so each (row, chunk) can be
+        //     computed on its own; fold_coef's mixing factors depend only on
+        //     that max and the chunk's own.
+        for (int i = tid; i < cn * rv; i += nth) {
+            const int c = i / rv, r = i % rv;
+            float mprev = s_run[2 * r];
+            for (int c2 = 0; c2 < c; ++c2)
+                mprev = fmaxf(mprev, s_ml[(c2 * rv + r) * 2]);
+            const Fold f = fold_coef(mprev, 0.f, s_ml[(c * rv + r) * 2], 0.f);
+            s_cf[(c * rv + r) * 2] = f.sa;
+            s_cf[(c * rv + r) * 2 + 1] = f.sc;
+            s_md[c * rv + r] = f.mode;
         }
         __syncthreads();
-        // (b) per-row coefficient chains
-        for (int r = tid; r < rv; r += nth) {
-            float ma = s_run[2 * r], la = s_run[2 * r + 1];
-            for (int c = 0; c < cn; ++c) {
-                const Fold f = fold_coef(ma, la, s_ml[(c * rv + r) * 2], s_ml[(c * rv + r) * 2 + 1]);
-                s_cf[(c * rv + r) * 2] = f.sa;
-                s_cf[(c * rv + r) * 2 + 1] = f.sc;
-                s_md[c * rv + r] = f.mode;
-                ma = f.m;
-                la = f.l;
-            }
-            s_run[2 * r] = ma;
-            s_run[2 * r + 1] = la;
-        }
-        __syncthreads();
-        // (c) per-element folds, chunk order
+        // (c) the sequential parts, in chunk order: O per element, (m, l) per
+        //     row -- the same operations fold_coef / fold_elem perform
         for (int e = tid; e < rv * DH; e += nth) {
             const int r = e / DH;
+            const bool row_lead = (e % DH) == 0;  // also carries the row's (m, l)
             float oa = s_acc[e];
+            float ma = s_run[2 * r], la = s_run[2 * r + 1];
+#pragma unroll 4
             for (int c = 0; c < cn; ++c) {
                 Fold f;
                 f.sa = s_cf[(c * rv + r) * 2];
                 f.sc = s_cf[(c * rv + r) * 2 + 1];
                 f.mode = s_md[c * rv + r];
                 oa = fold_elem(oa, s_o[c * rv * DH + e], f);
+                if (row_lead) {
+                    const float mc = s_ml[(c * rv + r) * 2], lc = s_ml[(c * rv + r) * 2 + 1];
+                    if (f.mode == 1) {
+                        ma = mc;
+                        la = lc;
+                    } else if (f.mode == 2) {
+                        ma = fmaxf(ma, mc);
+                        la = __fadd_rn(__fmul_rn(la, f.sa), __fmul_rn(lc, f.sc));
+                    }
+                }
             }
             s_acc[e] = oa;
+            if (row_lead) {
+                s_run2[2 * r] = ma;
+                s_run2[2 * r + 1] = la;
+            }
+        }
+        __syncthreads();
+        for (int r = tid; r < rv; r += nth) {
+            s_run[2 * r] = s_run2[2 * r];
+            s_run[2 * r + 1] = s_run2[2 * r + 1];
         }
         __syncthreads();
     }
@@ -383,13 +413,14 @@ __device__ __forceinline__ int tile_chunks(const ReqMeta &m, int qt, int tq, int
 struct Unit {
     int b, kvh, qt, c;
     bool valid;  // false: this CTA has nothing to do
+    ReqMeta meta;
 };
 
 // Split-KV schedule: CTA i takes the i-th non-empty (request, KV head, query
 // tile, chunk) unit, so every CTA with work comes first in the grid.  A
 // request whose lengths are inconsistent gets one unit per (KV head, query
 // tile) that only writes NaN rows.  Uses all threads; scratch in `s_int`
-// (>= 34 ints).
+// (>= 38 ints).
 __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -429,16 +460,29 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
     const long long excl = (long long)wpre + incl - cnt;
     const long long target = blockIdx.x;
     if (cnt > 0 && target >= excl && target < excl + cnt) {
+        const ReqMeta m = read_meta(p, tid);  // cached: this thread just read it
         s_int[32] = tid;
         s_int[33] = (int)(target - excl);
+        s_int[34] = m.qs;
+        s_int[35] = m.qn;
+        s_int[36] = m.L;
+        s_int[37] = (m.sane ? 1 : 0) | (m.ok ? 2 : 0);
     }
     __syncthreads();
-    Unit u{0, 0, 0, 0, false};
+    Unit u;
+    u.valid = false;
     const int b = s_int[32];
     if (b < 0)
         return u;
     int r = s_int[33];
-    const ReqMeta m = read_meta(p, b);
+    ReqMeta m;
+    m.qs = s_int[34];
+    m.qn = s_int[35];
+    m.L = s_int[36];
+    m.sane = (s_int[37] & 1) != 0;
+    m.ok = (s_int[37] & 2) != 0;
+    u.meta = m;
+    u.c = 0;
     const int qtl = (m.qn + p.tq - 1) / p.tq;
     u.b = b;
     u.valid = true;
@@ -485,8 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     static_assert(NBARS * 8 <= 512, "barrier area");
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived by indexing the shared array so the
+    // compiler keeps every access in the shared state space
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;
     uint8_t *sK = sQ + TILE_BYTES;
     uint8_t *sV = sK + NSK * TILE_BYTES;
@@ -506,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
     // ---------------------------------------------------------- work unit --
     int b, kvh, qt, c_grid = 0;
+    ReqMeta meta;
     if (p.split) {
         const Unit un = split_unit(p, CHUNK_DIV, reinterpret_cast<int *>(s_x));
         if (!un.valid)
@@ -514,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         kvh = un.kvh;
         qt = un.qt;
         c_grid = un.c;
+        meta = un.meta;
     } else {
         // longest work first: later query tiles see more keys
         const long long u = blockIdx.x;
@@ -521,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         qt = p.qtiles - 1 - (int)(u / nbh);
         kvh = (int)((u % nbh) % p.hkv);
         b = (int)((u % nbh) / p.hkv);
+        meta = read_meta(p, b);
     }
-    const ReqMeta meta = read_meta(p, b);
     const int qs = meta.qs, qn = meta.qn, L = meta.L;
     const int tok0 = qt * p.tq;
     if (!meta.ok) {
@@ -555,6 +602,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int64_t unit_q = ((int64_t)b * p.hkv + kvh) * p.qtiles + qt;
     const int64_t rec_floats = part_record_floats(p.ws_rows, DH);
     const int64_t rec_hdr = part_header_floats(p.ws_rows);
+
+    // The producer's first 16 block ids (two tiles) are requested before the
+    // set-up barrier so the load overlaps it.
+    auto load16 = [&](int t) {
+        const int pg = t * 8 + lane;
+        return (lane < 16 && pg < npages_need) ? __ldg(bt_row + pg) : 0;
+    };
+    int ids_cur = (warp == 0) ? load16(t_begin) : 0;
 
     // -------------------------------------------------------------- setup --
     if (tid == 0) {
@@ -606,16 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (lane < NKB)
             tma_load_3d(smem_addr(sQ + lane * 16384), &p.tm_q, bar(B_Q), lane * 64, kvh * p.group,
                         (int)tok_first);
-        auto load_id = [&](int t) {
-            const int pg = t * 8 + lane;
-            return (lane < 8 && pg < npages_need) ? __ldg(bt_row + pg) : 0;
-        };
-        int id_next = load_id(t_begin);
+        // ids of tiles (2j, 2j+1) sit in lanes 0-15 of ids_cur; the next pair is
+        // requested one pair ahead
+        int ids_next = 0;
         for (int it = 0; ok && it < n_it; ++it) {
             const int t = t_begin + it;
-            int id = id_next;
-            if (it + 1 < n_it)
-                id_next = load_id(t + 1);
+            if ((it & 1) == 0) {
+                if (it > 0)
+                    ids_cur = ids_next;
+                if (it + 2 < n_it)
+                    ids_next = load16(t + 2);
+            }
+            int id = __shfl_sync(0xffffffffu, ids_cur, (it & 1) * 8 + (lane & 7));
             const int np = min(8, npages_need - t * 8);
             const bool badl = lane < np && (id < 0 || (int64_t)id >= p.num_blocks);
             if (badl)
@@ -777,18 +834,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             tc_fence_after();
             const int nallow = row_valid ? max(0, min(64, pos - t * kKeys - 64 * h + 1)) : 0;
             const uint32_t scol = tmem + lane_off + sb * kKeys + 64 * h;  // this half's S columns
-            // pass 1: tile max over allowed keys of this half
+            // pass 1: max of the raw scores over allowed keys of this half
+            // (scale > 0, so this is the max of the scaled scores as well)
+            const bool unmasked = __all_sync(0xffffffffu, nallow == 64);
             float pmax = -INFINITY;
             if (warp_active && okw) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(scol, v0);
+                tmem_ld32(scol + 32, v1);
+                tmem_wait_ld();
+                if (unmasked) {
 #pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2) {
-                    uint32_t v[32];
-                    tmem_ld32(scol + g2 * 32, v);
-                    tmem_wait_ld();
+                    for (int i = 0; i < 32; ++i)
+                        pmax = fmaxf(pmax, fmaxf(__uint_as_float(v0[i]), __uint_as_float(v1[i])));
+                } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float s2 = __fmul_rn(__uint_as_float(v[i]), p.scale_log2);
-                        pmax = (g2 * 32 + i < nallow) ? fmaxf(pmax, s2) : pmax;
+                        pmax = (i < nallow) ? fmaxf(pmax, __uint_as_float(v0[i])) : pmax;
+                        pmax = (32 + i < nallow) ? fmaxf(pmax, __uint_as_float(v1[i])) : pmax;
                     }
                 }
             }
@@ -797,7 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 failed = true;
                 break;
             }
-            const float tmax = fmaxf(xmax[r], xmax[kRows + r]);
+            // C2: the tile max in log2 units, one fp32 multiply
+            const float tmax = __fmul_rn(fmaxf(xmax[r], xmax[kRows + r]), p.scale_log2);
             float m_new = m, corr = 1.f;
             bool need = false;
             if (tmax != -INFINITY) {
@@ -809,9 +873,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                     need = true;
                 }
             }
-            // pass 2: p = exp2(s2 - m), the half's fixed-order sum, P as BF16
+            // pass 2: p = exp2(fma(S, scale*log2e, -m)), the half's fixed-order
+            // sum, P as BF16
             float hs = 0.f;
             if (warp_active) {
+                const float negm = -m_new;
+                const float c2 = p.scale_log2;
                 float a[8];
                 uint32_t w[32];
 #pragma unroll
@@ -822,10 +889,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         const int c = g2 * 32 + i;
-                        const float s0 = __fmul_rn(__uint_as_float(v[i]), p.scale_log2);
-                        const float s1 = __fmul_rn(__uint_as_float(v[i + 1]), p.scale_log2);
-                        const float e0 = (c < nallow) ? ex2(__fsub_rn(s0, m_new)) : 0.f;
-                        const float e1 = (c + 1 < nallow) ? ex2(__fsub_rn(s1, m_new)) : 0.f;
+                        float e0 = ex2(__fmaf_rn(__uint_as_float(v[i]), c2, negm));
+                        float e1 = ex2(__fmaf_rn(__uint_as_float(v[i + 1]), c2, negm));
+                        if (!unmasked) {
+                            e0 = (c < nallow) ? e0 : 0.f;
+                            e1 = (c + 1 < nallow) ? e1 : 0.f;
+                        }
                         if (c < 8) {
                             a[c & 7] = e0;
                             a[(c + 1) & 7] = e1;

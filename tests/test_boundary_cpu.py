@@ -89,6 +89,8 @@ def test_attention_validation(lib):
     assert _attn(lib, c, out=0) == pagedattn.PA_ERR_INVALID_ARG
     assert _attn(lib, c, lse=FAKE + 2) == pagedattn.PA_ERR_INVALID_ARG
     assert _attn(lib, c, scale=float("nan")) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, scale=-0.1) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, c, scale=0.0) == pagedattn.PA_ERR_INVALID_ARG
     assert _attn(lib, c, ws=0, ws_len=0) == pagedattn.PA_ERR_WORKSPACE
     assert _attn(lib, c, ws=FAKE, ws_len=ws - 1) == pagedattn.PA_ERR_WORKSPACE
     assert _attn(lib, c, ws=FAKE + 16, ws_len=ws) == pagedattn.PA_ERR_INVALID_ARG
