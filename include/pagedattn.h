@@ -178,6 +178,39 @@ PA_API pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t
                              size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * PagedAttention for callers that cannot allocate device memory.
+ *
+ * Some callers cannot call cudaMalloc at all: code that runs while a CUDA
+ * graph is being captured (allocation is not a capturable operation), or an
+ * engine whose device memory is entirely reserved by its own pool allocator
+ * and that therefore has no buffer to hand over as the workspace that
+ * pa_paged_attention wants.  This variant takes the same arguments minus the
+ * workspace and uses instead a scratch array built into the library: a
+ * file-scope device array of PA_NOALLOC_SCRATCH_BYTES bytes that every GPU
+ * which loads the library holds until the process exits.
+ *   - The paper (the source pages) has no counterpart to this entry point.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *     routine.  It clears the scratch's arrival counters with
+ *     cudaMemsetAsync on `stream`, then launches the same kernel as
+ *     pa_paged_attention with the scratch as its workspace.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - If the bounds need more scratch than PA_NOALLOC_SCRATCH_BYTES (see
+ *     pa_paged_attention_workspace_size), it returns PA_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - Every call on a device shares the one array: calls that may overlap on
+ *     the GPU (different streams without ordering) race on it.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+PA_API pa_status pa_paged_attention_noalloc(const void *q, int64_t num_q_tokens, int64_t q_tok_stride,
+                                            int32_t num_q_heads, const pa_kv_cache *cache,
+                                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                            const int32_t *seq_lens, const int32_t *query_start_loc,
+                                            int32_t num_seqs, int32_t max_query_len, int32_t max_seq_len,
+                                            float scale, void *out, float *lse, pa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * flag.  Returns PA_OK, PA_ERR_BAD_METADATA or PA_ERR_TIMEOUT (or
  * PA_ERR_CUDA if the synchronisation failed).  *first_bad_index (may be

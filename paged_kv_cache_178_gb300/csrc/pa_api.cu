@@ -278,6 +278,51 @@ pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_
     return cuda_status(e);
 }
 
+// Scratch for pa_paged_attention_noalloc: lives in the library image, so
+// every device that loads the library holds it; nothing is allocated per call.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+static void *g_noalloc_ptr[kMaxDevices];
+
+pa_status pa_paged_attention_noalloc(const void *q, int64_t num_q_tokens, int64_t q_tok_stride,
+                                     int32_t num_q_heads, const pa_kv_cache *cache,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                                     int32_t max_query_len, int32_t max_seq_len, float scale, void *out,
+                                     float *lse, pa_stream_t stream)
+{
+    if (!cache)
+        return PA_ERR_INVALID_ARG;
+    AttnPlan pl;
+    if (plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
+                       &pl) &&
+        pl.ws_bytes > PA_NOALLOC_SCRATCH_BYTES)
+        return PA_ERR_WORKSPACE;  // these bounds need more scratch than the built-in array holds
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PA_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        // Host code cannot use the array's name as a device address: resolve
+        // it once per device, with that device current.
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+                return PA_ERR_CUDA;
+            g_noalloc_ptr[dev] = ptr;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    // The arrival counters at the head of the scratch must start at zero; the
+    // previous call (or an aborted one) may have left anything there.
+    if (pl.ws_counter_bytes > 0 &&
+        cudaMemsetAsync(scratch, 0, pl.ws_counter_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return pa_paged_attention(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables, max_blocks_per_seq,
+                              seq_lens, query_start_loc, num_seqs, max_query_len, max_seq_len, scale, out, lse,
+                              scratch, PA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 pa_status pa_check_errors(pa_stream_t stream, int64_t *first_bad_index)
 {
     if (first_bad_index)

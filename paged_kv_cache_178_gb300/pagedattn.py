@@ -34,7 +34,9 @@ PA_ERR_TIMEOUT = 5
 PA_ERR_CUDA = 6
 
 EXPORTED = ("pa_init", "pa_reshape_and_cache", "pa_paged_attention_workspace_size",
-            "pa_paged_attention", "pa_check_errors", "pa_status_string", "pa_last_launch_info")
+            "pa_paged_attention", "pa_paged_attention_noalloc", "pa_check_errors",
+            "pa_status_string", "pa_last_launch_info")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class PaKvCache(ctypes.Structure):
@@ -75,6 +77,9 @@ def load(path: str = LIB_PATH):
         lib.pa_paged_attention.restype = i32
         lib.pa_paged_attention.argtypes = [vp, i64, i64, i32, ctypes.POINTER(PaKvCache), vp, i32, vp,
                                            vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+        lib.pa_paged_attention_noalloc.restype = i32
+        lib.pa_paged_attention_noalloc.argtypes = [vp, i64, i64, i32, ctypes.POINTER(PaKvCache), vp, i32,
+                                                   vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
         lib.pa_check_errors.restype = i32
         lib.pa_check_errors.argtypes = [vp, ctypes.POINTER(i64)]
         lib.pa_status_string.restype = ctypes.c_char_p
@@ -199,6 +204,25 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
         lse.data_ptr() if lse is not None else 0, ws_ptr, ws_len, _stream_handle(stream)),
         "pa_paged_attention")
     return out, lse
+
+
+def paged_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                            query_start_loc: torch.Tensor, scale: float, max_query_len: int,
+                            max_seq_len: int, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None) -> int:
+    """paged_attention for callers that cannot allocate: no workspace and no
+    output allocation here (out, and lse if wanted, are passed in); the
+    library's built-in scratch array is used instead.  Returns the status
+    code (PA_ERR_WORKSPACE when the bounds need more than
+    NOALLOC_SCRATCH_BYTES) rather than raising."""
+    c = cache_struct(k_cache, v_cache)
+    tq, hq, dh = q.shape
+    return int(load().pa_paged_attention_noalloc(
+        q.data_ptr(), tq, q.stride(0), hq, ctypes.byref(c), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), seq_lens.numel(),
+        int(max_query_len), int(max_seq_len), float(scale), out.data_ptr(),
+        lse.data_ptr() if lse is not None else 0, _stream_handle(stream)))
 
 
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
