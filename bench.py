@@ -295,8 +295,9 @@ def run_ours(args, ws, rank, local):
     pagedattn.init()
     stream = torch.cuda.Stream(device=dev)
     peaks, peak_src = load_peaks()
-    if args.workload == "prefill":
-        pf = measure_prefill(args, dev, stream, ws, peaks, peak_src, launches=args.steps)
+    if args.workload in ("prefill", "wide"):
+        pf = measure_prefill(args, dev, stream, ws, peaks, peak_src, launches=args.steps,
+                             wide=args.workload == "wide")
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": pf["tflops"], "unit": "TFLOP/s",
                               "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
@@ -387,6 +388,8 @@ def run_ours(args, ws, rank, local):
     }
     if not args.no_secondary:
         line["prefill"] = measure_prefill(args, dev, stream, ws, peaks, peak_src)
+        line["prefill_wide"] = measure_prefill(args, dev, stream, ws, peaks, peak_src, launches=20,
+                                               wide=True)
     if not args.no_e2e:
         line["e2e"] = measure_e2e(args, w, reps, dev, kv_bytes, ws)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -397,12 +400,13 @@ def run_ours(args, ws, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200):
-    """Long causal prefill B=1 Q=KV=4096 Dh=128: attention launches alone,
-    4 rotating replicas; TFLOP/s over causal algorithmic flops."""
+def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200, wide: bool = False):
+    """Causal prefill, attention launches alone over rotating replicas;
+    TFLOP/s over causal algorithmic flops.  Default: B=1 Q=KV=4096 Dh=128;
+    wide: B=1 Q=KV=18432 Hq=16 Hkv=2 Dh=512."""
     from paged_kv_cache_178_gb300 import pagedattn
     from paged_kv_cache_178_gb300.device import DeviceWorkload
-    w = wl.long_prefill(4096)
+    w = wl.wide_head(18432) if wide else wl.long_prefill(4096)
     reps = [DeviceWorkload(w, device=str(dev), fill_bits=None) for _ in range(4)]
     for dw in reps:
         dw.write_cache()
@@ -423,7 +427,9 @@ def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200)
     t = time_graphed(g, n, stream, ws) / n
     flops = causal_flops(w)
     tf = flops / t / 1e12
-    return {"workload": "causal prefill B=1 Q=KV=4096 Hq=8 Hkv=2 Dh=128", "tflops": round(tf, 2),
+    name = ("causal prefill B=1 Q=KV=18432 Hq=16 Hkv=2 Dh=512" if wide
+            else "causal prefill B=1 Q=KV=4096 Hq=8 Hkv=2 Dh=128")
+    return {"workload": name, "tflops": round(tf, 2),
             "us_per_launch": round(t * 1e6, 2), "flops_per_launch": flops,
             "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4),
             "peak_source": f"{peak_src} bf16_tflops (burst)", "schedule": info}
@@ -592,8 +598,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
-                    help="decode (default, the headline) or the long causal prefill alone")
+    ap.add_argument("--workload", choices=["decode", "prefill", "wide"], default="decode",
+                    help="decode (default, the headline), or one causal prefill alone: "
+                         "prefill (Dh=128, 4096) or wide (Dh=512, 18432)")
     ap.add_argument("--replicas", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")

@@ -235,8 +235,6 @@ pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_
     if (!plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
                         &pl))
         return PA_ERR_UNSUPPORTED;
-    if (cache->head_dim == 512)
-        return PA_ERR_UNSUPPORTED;
     if (pl.ws_bytes > 0) {
         if (!workspace || workspace_bytes < pl.ws_bytes)
             return PA_ERR_WORKSPACE;

@@ -1,0 +1,557 @@
+// K2 for head dim 512: a two-CTA cluster per 128-row tile.
+//
+// A 128 x 512 FP32 output accumulator alone would fill a CTA's 512 TMEM
+// columns, so the head dimension is split across a CTA pair ("harden compact
+// peer-local KV prefill for Gemma-4", Scope: Hq=16, Hkv=2, d=512; here both
+// CTAs of the pair sit on one GPU).  CTA rank c of the pair owns columns
+// [256c, 256c+256) of Q, K, V and O:
+//   - its Q half lives in TMEM (BF16, two per column) and is the A operand of
+//     S_c = Q_c . K_c^T, the partial scores over its 256 columns;
+//   - each CTA writes its partial S into the peer's shared memory (DSMEM) and
+//     reads the peer's, then both form S = S_0 + S_1 (IEEE addition is
+//     commutative, so both CTAs hold the same bits) and run the identical
+//     softmax, so P, m and l agree bit for bit across the pair;
+//   - O_c += P . V_c (N = 256) accumulates in the CTA's own TMEM.
+// Warp roles and the fixed arithmetic follow the head-dim 128/256 kernel,
+// with KV tiles of 64 keys (C1 at head dim 512) and 32-column softmax halves:
+//   tile sum = (8-way interleaved sum of the half's 32 columns) for each half,
+//   half0 + half1; one chunk per row (no split-KV at head dim 512).
+#include <cstdio>
+#include <cstring>
+
+#include "pa_attn_common.cuh"
+
+namespace pa {
+
+namespace d512 {
+
+constexpr int kKeys = 64;               // keys per KV tile
+constexpr int kHalfCols = 256;          // head-dim columns per CTA of the pair
+constexpr int kNKB = kHalfCols / 64;    // 64-column blocks per half
+constexpr int kTileBytes = kNKB * kKeys * 128;  // one KV half tile (32 KB)
+constexpr int kStagesK = 2, kStagesV = 2;
+constexpr int kXStride = 68;            // floats per exchanged row (64 + 4 pad: conflict-free)
+constexpr int kXBytes = kRows * kXStride * 4;
+constexpr int kSmallBytes = 512 + 64 + 2 * 2 * kRows * 4 + kRows * 2 * 4;
+constexpr uint32_t kQCol = 0;           // TMEM: Q half (128 columns of BF16 pairs)
+constexpr uint32_t kSCol = 128;         // TMEM: two S/P buffers of 64 columns
+constexpr uint32_t kOCol = 256;         // TMEM: O half (256 columns)
+
+constexpr size_t smem_bytes()
+{
+    return 1024 + (size_t)kTileBytes * (kStagesK + kStagesV) + 2 * (size_t)kXBytes + kSmallBytes;
+}
+
+}  // namespace d512
+
+// Bounded wait for a phase completed by the peer CTA (acquire at cluster
+// scope).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                 ErrState *err, int where)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            record_error(err, kErrTimeout, ((long long)blockIdx.x << 8) | where);
+            return false;
+        }
+    }
+    return true;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kernel(const __grid_constant__ AttnParams p)
+{
+    using namespace d512;
+    constexpr int DH = 512;
+    constexpr int NSK = kStagesK, NSV = kStagesV;
+    constexpr uint32_t ID_QK = idesc_bf16_f32(kRows, kKeys, false);
+    constexpr uint32_t ID_PV = idesc_bf16_f32(kRows, kHalfCols, true);
+    constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
+    constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_XF = B_PV + 2, B_XE = B_XF + 2;
+    constexpr int B_FIN = B_XE + 2, B_PROD = B_FIN + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
+    static_assert(NBARS * 8 <= 512, "barrier area");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sK = smem;
+    uint8_t *sV = sK + NSK * kTileBytes;
+    float *sX = reinterpret_cast<float *>(sV + NSV * kTileBytes);   // [2][128][kXStride]
+    uint8_t *small = reinterpret_cast<uint8_t *>(sX) + 2 * kXBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small);
+    int *sflags = reinterpret_cast<int *>(small + 512);  // [0] abort [1] tmem [3] bad
+    float *s_x = reinterpret_cast<float *>(small + 512 + 64);   // [2 exchanges][2 halves][128]
+    float *s_ml = s_x + 2 * 2 * kRows;                          // [128][2]
+    volatile int *abort_flag = sflags;
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    auto wb = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, abort_flag, p.err, i); };
+    auto wbc = [&](int i, uint32_t parity) { return wait_bar_cluster(bar(i), parity, abort_flag, p.err, i); };
+    const int tid = threadIdx.x;
+    const int warp = tid / 32, lane = tid % 32;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t peer = crank ^ 1u;
+
+    // ---------------------------------------------------------- work unit --
+    // both CTAs of a pair take the same unit, longest work first
+    const long long u = blockIdx.x >> 1;
+    const long long nbh = (long long)p.num_seqs * p.hkv;
+    const int qt = p.qtiles - 1 - (int)(u / nbh);
+    const int kvh = (int)((u % nbh) % p.hkv);
+    const int b = (int)((u % nbh) / p.hkv);
+    const ReqMeta meta = read_meta(p, b);
+    const int qs = meta.qs, qn = meta.qn, L = meta.L;
+    const int tok0 = qt * p.tq;
+    if (!meta.ok) {
+        if (crank == 0) {
+            if (qt == p.qtiles - 1 && tid == 0)
+                record_error(p.err, kErrBadMetadata, b);
+            if (meta.sane && tok0 < qn)
+                write_nan_rows<DH>(p, (int64_t)qs + tok0, min(p.tq, qn - tok0), kvh);
+        }
+        return;
+    }
+    if (tok0 >= qn)
+        return;
+    const int ntok = min(p.tq, qn - tok0);
+    const int rows_valid = ntok * p.group;
+    const int64_t tok_first = (int64_t)qs + tok0;
+    const int kend = L - qn + tok0 + ntok;
+    const int n_it = (kend + kKeys - 1) / kKeys;
+    const int npages_need = (kend + 15) / 16;
+    const int32_t *bt_row = p.block_tables + (int64_t)b * p.max_blocks;
+    auto load8 = [&](int t) {  // block ids of tiles t and t+1 (4 pages each)
+        const int pg = t * 4 + lane;
+        return (lane < 8 && pg < npages_need) ? __ldg(bt_row + pg) : 0;
+    };
+    int ids_cur = (warp == 0) ? load8(0) : 0;
+
+    // -------------------------------------------------------------- setup --
+    if (tid == 0) {
+        mbar_init(bar(B_Q), 4);
+        for (int s = 0; s < NSK; ++s) {
+            mbar_init(bar(B_KF + s), 1);
+            mbar_init(bar(B_KE + s), 1);
+        }
+        for (int s = 0; s < NSV; ++s) {
+            mbar_init(bar(B_VF + s), 1);
+            mbar_init(bar(B_VE + s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_SF + i), 1);
+            mbar_init(bar(B_PF + i), 8);
+            mbar_init(bar(B_PV + i), 1);
+            mbar_init(bar(B_XF + i), 256);  // the peer's 256 softmax threads wrote their rows
+            mbar_init(bar(B_XE + i), 256);  // the peer's 256 softmax threads read what we wrote
+        }
+        mbar_init(bar(B_FIN), 8);
+        mbar_init(bar(B_PROD), 1);
+        mbar_init(bar(B_DONE), 1);
+        sflags[0] = 0;
+        sflags[3] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&sflags[1]), 512);
+        tmem_relinquish();
+    }
+    if (tid == 64) {
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+    }
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = static_cast<uint32_t>(sflags[1]);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer --
+        bool ok = true, any_bad = false;
+        int last_k_use[NSK], last_v_use[NSV];
+        for (int s = 0; s < NSK; ++s) last_k_use[s] = -1;
+        for (int s = 0; s < NSV; ++s) last_v_use[s] = -1;
+        int ids_next = 0;
+        for (int it = 0; ok && it < n_it; ++it) {
+            if ((it & 1) == 0) {
+                if (it > 0)
+                    ids_cur = ids_next;
+                if (it + 2 < n_it)
+                    ids_next = load8(it + 2);
+            }
+            int id = __shfl_sync(0xffffffffu, ids_cur, (it & 1) * 4 + (lane & 3));
+            const int np = min(4, npages_need - it * 4);
+            const bool badl = lane < np && (id < 0 || (int64_t)id >= p.num_blocks);
+            if (badl)
+                id = 0;
+            any_bad |= __any_sync(0xffffffffu, badl);
+            const int my_page = lane / kNKB, my_kb = lane % kNKB;
+            const int my_id = __shfl_sync(0xffffffffu, id, my_page & 3);
+            const bool issue = lane < np * kNKB;
+            const int col = (int)crank * kHalfCols + my_kb * 64;
+            const int sk = it % NSK, uk = it / NSK;
+            if (lane == 0) {
+                if (uk >= 1)
+                    ok = wb(B_KE + sk, (uk - 1) & 1);
+                if (ok)
+                    mbar_arrive_expect_tx(bar(B_KF + sk), np * kNKB * 2048);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            if (issue)
+                tma_load_4d(smem_addr(sK + sk * kTileBytes + my_kb * 8192 + my_page * 2048), &p.tm_k,
+                            bar(B_KF + sk), col, kvh, 0, my_id);
+            last_k_use[sk] = uk;
+            const int sv = it % NSV, uv = it / NSV;
+            if (lane == 0) {
+                if (uv >= 1)
+                    ok = wb(B_VE + sv, (uv - 1) & 1);
+                if (ok)
+                    mbar_arrive_expect_tx(bar(B_VF + sv), np * kNKB * 2048);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            if (issue)
+                tma_load_4d(smem_addr(sV + sv * kTileBytes + my_kb * 8192 + my_page * 2048), &p.tm_v,
+                            bar(B_VF + sv), col, kvh, 0, my_id);
+            last_v_use[sv] = uv;
+        }
+        if (lane == 0) {
+            if (any_bad) {
+                record_error(p.err, kErrBadMetadata, b);
+                sflags[3] = 1;
+            }
+            mbar_arrive(bar(B_PROD));
+            if (!ok) {
+                for (int s = 0; s < NSK; ++s)
+                    if (last_k_use[s] >= 0)
+                        wait_bar_drain(bar(B_KF + s), last_k_use[s] & 1);
+                for (int s = 0; s < NSV; ++s)
+                    if (last_v_use[s] >= 0)
+                        wait_bar_drain(bar(B_VF + s), last_v_use[s] & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer --
+        bool ok = true;
+        if (lane == 0)
+            ok = wb(B_Q, 0);  // Q half in TMEM
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        auto issue_pv = [&](int j) -> bool {
+            const int sv = j % NSV;
+            bool okj = __all_sync(0xffffffffu, wb(B_VF + sv, (j / NSV) & 1));
+            if (!okj)
+                return false;
+            if ((j + 1) * kKeys > kend) {
+                const int row0 = kend - j * kKeys;
+                const int nz = (kKeys - row0) * kNKB * 8;
+                uint8_t *vs = sV + sv * kTileBytes;
+                for (int idx = lane; idx < nz; idx += 32) {
+                    const int row = row0 + idx / (kNKB * 8);
+                    const int rem = idx % (kNKB * 8);
+                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * 8192 + row * 128 + (rem % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) {
+                okj = wb(B_PF + (j & 1), (j >> 1) & 1);
+                if (okj) {
+                    tc_fence_after();
+                    const uint32_t pcol = tmem + kSCol + (uint32_t)(j & 1) * kKeys;
+                    const uint32_t vbase = smem_addr(sV + sv * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        const uint64_t bd = sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+                        mma_bf16_ts(tmem + kOCol, pcol + kk * 8, bd, ID_PV, (kk > 0 || j > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(B_VE + sv));
+                    mma_commit(bar(B_PV + (j & 1)));
+                }
+            }
+            return __shfl_sync(0xffffffffu, okj, 0);
+        };
+        for (int it = 0; ok && it <= n_it; ++it) {
+            if (it < n_it) {
+                const int sk = it % NSK;
+                if (lane == 0) {
+                    ok = wb(B_KF + sk, (it / NSK) & 1);
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t kbase = smem_addr(sK + sk * kTileBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kHalfCols / 16; ++kk) {
+                            const uint64_t bd = sdesc_sw128(kbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
+                            mma_bf16_ts(tmem + kSCol + (uint32_t)(it & 1) * kKeys, tmem + kQCol + kk * 8, bd, ID_QK,
+                                        kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(B_KE + sk));
+                        mma_commit(bar(B_SF + (it & 1)));
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            if (ok && it >= 1)
+                ok = issue_pv(it - 1);
+        }
+        if (lane == 0) {
+            mma_commit(bar(B_DONE));
+            wait_bar_drain(bar(B_DONE), 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 12) {
+        // --------------------------------------- softmax (2 halves, pair) --
+        const int h = (warp - 4) / 4;
+        const int q4 = warp % 4;
+        const int r = q4 * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const bool row_valid = r < rows_valid;
+        const bool warp_active = 32 * q4 < rows_valid;
+        const int pos = L - qn + tok0 + r / p.group;
+        float *xmax = s_x;
+        float *xsum = s_x + 2 * kRows;
+        float m = -INFINITY, l = 0.f;
+        bool failed = false;
+        for (int it = 0; it < n_it; ++it) {
+            const int sb = it & 1;
+            // own partial S -> the peer's exchange buffer, then the peer's -> ours
+            bool okw = !failed && wb(B_SF + sb, (it >> 1) & 1);
+            if (okw && it >= 2)
+                okw = wbc(B_XE + sb, ((it >> 1) - 1) & 1);  // the peer has read what we wrote two tiles ago
+            okw = __all_sync(0xffffffffu, okw);
+            tc_fence_after();
+            const uint32_t scol = tmem + lane_off + kSCol + sb * kKeys + 32 * h;
+            uint32_t v[32];
+            if (okw) {
+                tmem_ld32(scol, v);
+                tmem_wait_ld();
+                const uint32_t dst = mapa_shared(smem_addr(sX + (sb * kRows + r) * kXStride + 32 * h), peer);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    st_cluster_v4(dst + 16 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                mbar_arrive_cluster(mapa_shared(bar(B_XF + sb), peer));
+                okw = wbc(B_XF + sb, (it >> 1) & 1);
+            }
+            okw = __all_sync(0xffffffffu, okw);
+            float s[32];
+            if (okw) {
+                const float4 *src = reinterpret_cast<const float4 *>(sX + (sb * kRows + r) * kXStride + 32 * h);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 x = src[i];
+                    s[4 * i + 0] = __fadd_rn(__uint_as_float(v[4 * i + 0]), x.x);
+                    s[4 * i + 1] = __fadd_rn(__uint_as_float(v[4 * i + 1]), x.y);
+                    s[4 * i + 2] = __fadd_rn(__uint_as_float(v[4 * i + 2]), x.z);
+                    s[4 * i + 3] = __fadd_rn(__uint_as_float(v[4 * i + 3]), x.w);
+                }
+                mbar_arrive_cluster(mapa_shared(bar(B_XE + sb), peer));  // our buffer sb is free again
+            }
+            const int nallow = row_valid ? max(0, min(32, pos - it * kKeys - 32 * h + 1)) : 0;
+            float pmax = -INFINITY;
+            if (okw && warp_active) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pmax = (i < nallow) ? fmaxf(pmax, s[i]) : pmax;
+            }
+            xmax[h * kRows + r] = pmax;
+            if (named_sync_or(1, 256, !okw)) {
+                failed = true;
+                break;
+            }
+            const float tmax = __fmul_rn(fmaxf(xmax[r], xmax[kRows + r]), p.scale_log2);
+            float m_new = m, corr = 1.f;
+            bool need = false;
+            if (tmax != -INFINITY) {
+                if (m == -INFINITY) {
+                    m_new = tmax;
+                } else if (tmax > __fadd_rn(m, kTau)) {
+                    m_new = tmax;
+                    corr = ex2(__fsub_rn(m, m_new));
+                    need = true;
+                }
+            }
+            float hs = 0.f;
+            if (warp_active) {
+                const float negm = -m_new;
+                float a[8];
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float e0 = (i < nallow) ? ex2(__fmaf_rn(s[i], p.scale_log2, negm)) : 0.f;
+                    float e1 = (i + 1 < nallow) ? ex2(__fmaf_rn(s[i + 1], p.scale_log2, negm)) : 0.f;
+                    if (i < 8) {
+                        a[i & 7] = e0;
+                        a[(i + 1) & 7] = e1;
+                    } else {
+                        a[i & 7] = __fadd_rn(a[i & 7], e0);
+                        a[(i + 1) & 7] = __fadd_rn(a[(i + 1) & 7], e1);
+                    }
+                    w[i / 2] = pack_bf16x2(e0, e1);
+                }
+                hs = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
+                               __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
+                // P of keys [32h, 32h+32) -> columns [16h, 16h+16) of this S buffer
+                tmem_st16(tmem + lane_off + kSCol + sb * kKeys + 16 * h, w);
+            }
+            xsum[h * kRows + r] = hs;
+            named_sync(1, 256);
+            const float tsum = __fadd_rn(xsum[r], xsum[kRows + r]);
+            bool okr = true;
+            if (__any_sync(0xffffffffu, need)) {
+                okr = __all_sync(0xffffffffu, wb(B_PV + ((it - 1) & 1), ((it - 1) >> 1) & 1));
+                failed = !okr;
+            }
+            if (__any_sync(0xffffffffu, need) && okr) {
+                tc_fence_after();
+                const float f = need ? corr : 1.f;
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t o[32];
+                    const uint32_t c = tmem + lane_off + kOCol + 128 * h + g * 32;
+                    tmem_ld32(c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), f));
+                    tmem_st32(c, o);
+                }
+            }
+            tmem_wait_st();
+            l = need ? __fadd_rn(__fmul_rn(l, corr), tsum) : __fadd_rn(l, tsum);
+            m = m_new;
+            const bool last = (it == n_it - 1);
+            if (last && h == 0) {
+                s_ml[r * 2] = m;
+                s_ml[r * 2 + 1] = l;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_PF + sb));
+                if (last)
+                    mbar_arrive(bar(B_FIN));
+            }
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------ Q into TMEM, then epilogue --
+        const int q4 = warp % 4;
+        const int r = q4 * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const bool row_valid = r < rows_valid;
+        const int G = p.group;
+        const int64_t tok = tok_first + r / G;
+        const int head = kvh * G + r % G;
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const __nv_bfloat16 *>(p.q) + tok * p.q_tok_stride + (int64_t)head * DH +
+                (int)crank * kHalfCols);
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 x = row_valid ? __ldg(src + g * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * i] = x.x;
+                    w[4 * i + 1] = x.y;
+                    w[4 * i + 2] = x.z;
+                    w[4 * i + 3] = x.w;
+                }
+                tmem_st32(tmem + lane_off + kQCol + g * 32, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_Q));
+        }
+        bool ok = wb(B_FIN, 0);
+        if (ok)
+            ok = wb(B_PV + ((n_it - 1) & 1), ((n_it - 1) >> 1) & 1);
+        if (ok)
+            ok = wb(B_PROD, 0);
+        if (__all_sync(0xffffffffu, ok)) {
+            tc_fence_after();
+            const float mr = s_ml[r * 2], lr = s_ml[r * 2 + 1];
+            const bool bad = sflags[3] != 0;
+            const float inv = __frcp_rn(lr);
+#pragma unroll 1
+            for (int g = 0; g < kHalfCols / 32; ++g) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + kOCol + g * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = bad ? 0x7FC00000u : __float_as_uint(__fmul_rn(__uint_as_float(o[i]), inv));
+                if (row_valid)
+                    store_out32(p.out + (tok * p.hq + head) * DH + (int)crank * kHalfCols + g * 32, o);
+            }
+            if (row_valid && crank == 0 && p.lse)
+                p.lse[tok * p.hq + head] = bad ? __int_as_float(0x7FC00000) : lse_of(mr, lr);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    // neither CTA leaves while the peer may still write into its shared
+    // memory or arrive on its barriers
+    cluster_sync_all();
+}
+
+cudaError_t init_attention512_attributes()
+{
+    return cudaFuncSetAttribute(attn512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)d512::smem_bytes());
+}
+
+cudaError_t launch_attention512(const AttnArgs &a, const AttnPlan &pl, ErrState *err, cudaStream_t stream)
+{
+    AttnParams p;
+    memset(&p, 0, sizeof(p));
+    {
+        const cuuint64_t dims[4] = {512, (cuuint64_t)a.num_kv_heads, 16, (cuuint64_t)a.num_blocks};
+        const cuuint64_t strides[3] = {(cuuint64_t)a.head_stride * 2, (cuuint64_t)a.token_stride * 2,
+                                       (cuuint64_t)a.block_stride * 2};
+        const cuuint32_t box[4] = {64, 1, 16, 1};
+        if (encode_tiled(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.k), dims, strides,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if (encode_tiled(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.v), dims, strides,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    p.q = a.q;
+    p.q_tok_stride = a.q_tok_stride;
+    p.block_tables = a.block_tables;
+    p.seq_lens = a.seq_lens;
+    p.qsl = a.query_start_loc;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.lse = a.lse;
+    p.err = err;
+    p.num_q_tokens = a.num_q_tokens;
+    p.num_blocks = a.num_blocks;
+    p.max_blocks = a.max_blocks_per_seq;
+    p.num_seqs = a.num_seqs;
+    p.hq = a.num_q_heads;
+    p.hkv = a.num_kv_heads;
+    p.group = pl.group;
+    p.tq = pl.tokens_per_tile;
+    p.qtiles = pl.qtiles;
+    p.nch = 1;
+    p.max_query_len = a.max_query_len;
+    p.max_seq_len = a.max_seq_len;
+    p.split = 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    attn512_kernel<<<(unsigned)pl.grid, 512, d512::smem_bytes(), stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -74,6 +74,10 @@ cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &plan, ErrState *
 
 cudaError_t init_attention_attributes();
 
+// Head dim 512: two-CTA clusters (pa_attn512.cu).
+cudaError_t init_attention512_attributes();
+cudaError_t launch_attention512(const AttnArgs &a, const AttnPlan &plan, ErrState *err, cudaStream_t stream);
+
 // Encodes a tiled tensor map (driver entry point fetched at run time).
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
                       const cuuint64_t *dims, const cuuint64_t *strides_bytes,

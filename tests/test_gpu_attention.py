@@ -288,3 +288,20 @@ def test_bound_violation_flags():
     st, idx = pagedattn.check_errors()
     assert st == pagedattn.PA_ERR_BAD_METADATA and idx == 0
     _bitwise(out[1:], o2[1:], "other requests after a bound violation")
+
+
+# ------------------------------------------------------- head dim 512 ----
+
+@pytest.mark.parametrize("L", [3072, 18432])
+def test_wide_head_dh512(L):
+    """Hq=16, Hkv=2, d=512 causal prefill (two-CTA pairs split the head dim)."""
+    w = wl.wide_head(L)
+    dw, out, lse = _run(w)
+    assert "in-cta-pair" in pagedattn.last_launch_info()
+    rows = _rows_sample(L, extra=(63, 64, 65, L // 2), k=24 if L > 8192 else 48)
+    _compare(w, out, lse, rows=rows)
+
+
+def test_wide_head_prefill_equals_decode():
+    w = wl.wide_head(3072)
+    _prefill_vs_decode(w, [0, 15, 16, 63, 64, 1000, 2047, 3071])

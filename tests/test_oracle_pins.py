@@ -133,7 +133,14 @@ def _mixed_workload():
                     seed=12)
 
 
-@pytest.mark.parametrize("make", [wl.composition, _mixed_workload])
+def _wide_small():
+    """Hq=16, Hkv=2 (G=8), Dh=512: the wide-head geometry at a small length."""
+    return wl.build("wide_small", num_q_heads=16, num_kv_heads=2, head_dim=512, seq_lens=[40, 17],
+                    query_lens=[40, 5], num_blocks=8, block_rows=[[5, 2, 7], [0, 3]],
+                    layout="interleaved", seed=41)
+
+
+@pytest.mark.parametrize("make", [wl.composition, _mixed_workload, _wide_small])
 def test_matches_dense_sdpa(make):
     w = make()
     out, lse = oracle_attention(w)
