@@ -48,7 +48,17 @@ from paged_kv_cache_178_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s, % of GB300 roofline"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_kernel_decode_b4_kv7168.md")
-KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_178_gb300", "csrc", "pa_attn.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_178_gb300", "csrc", f)
+                  for f in ("pa_attn.cu", "pa_attn_common.cuh", "pa_ptx.cuh")]
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of sha256 over the decode kernel's sources."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ ranks --
@@ -223,7 +233,7 @@ def profile_traffic():
     was taken on the current kernel source; else None."""
     try:
         text = open(PROFILE_SUMMARY).read()
-        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+        src = kernel_source_hash()
         m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
         m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
         if m_hash and m_bytes and m_hash.group(1) == src:
@@ -406,7 +416,7 @@ def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200,
     wide: B=1 Q=KV=18432 Hq=16 Hkv=2 Dh=512."""
     from paged_kv_cache_178_gb300 import pagedattn
     from paged_kv_cache_178_gb300.device import DeviceWorkload
-    w = wl.wide_head(18432) if wide else wl.long_prefill(4096)
+    w = wl.wide_head(args.wide_len) if wide else wl.long_prefill(4096)
     reps = [DeviceWorkload(w, device=str(dev), fill_bits=None) for _ in range(4)]
     for dw in reps:
         dw.write_cache()
@@ -427,7 +437,7 @@ def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200,
     t = time_graphed(g, n, stream, ws) / n
     flops = causal_flops(w)
     tf = flops / t / 1e12
-    name = ("causal prefill B=1 Q=KV=18432 Hq=16 Hkv=2 Dh=512" if wide
+    name = (f"causal prefill B=1 Q=KV={args.wide_len} Hq=16 Hkv=2 Dh=512" if wide
             else "causal prefill B=1 Q=KV=4096 Hq=8 Hkv=2 Dh=128")
     return {"workload": name, "tflops": round(tf, 2),
             "us_per_launch": round(t * 1e6, 2), "flops_per_launch": flops,
@@ -602,6 +612,8 @@ def main():
                     help="decode (default, the headline), or one causal prefill alone: "
                          "prefill (Dh=128, 4096) or wide (Dh=512, 18432)")
     ap.add_argument("--replicas", type=int, default=16)
+    ap.add_argument("--wide-len", type=int, default=18432,
+                    help="sequence length of the Dh=512 prefill (3072, 8192, 11264 or 18432)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
