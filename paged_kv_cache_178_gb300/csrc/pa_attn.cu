@@ -17,13 +17,17 @@
 //   warps 4-11   softmax, two halves: warps 4-7 own score columns 0-63, warps
 //                8-11 columns 64-127, one TMEM lane (row) per thread.
 //   warps 12-15  correction: chunk folds, epilogue, split partial states.
+// Prefill with two or more query tiles runs on CTA pairs that share each MMA
+// (cta_group::2, M = 256), so each CTA loads half of every K/V tile; the
+// single-CTA form serves split-KV decode and one-tile requests.
 //
 // Fixed arithmetic (same page, intro and Changes: one schedule for every
 // shape, no implicit FMA contraction).  Every row follows the same sequence
 // of operations whatever the batch, query length, other rows or launch
 // bounds, so prefill and decode agree bit for bit:
-//   C1  KV tiles of 128 keys aligned to key 0; one MMA shape (M=128, K-steps
-//       of 16 in ascending order, BF16 in, FP32 accumulate).
+//   C1  KV tiles of 128 keys aligned to key 0; K-steps of 16 in ascending
+//       order, BF16 in, FP32 accumulate (M = 128 per CTA, or 256 over a CTA
+//       pair: each output element is the same dot product either way).
 //   C2  c = scale*log2 e is formed once, in fp32, on the host (scale > 0).
 //       Tile max in log2 units: (max of the raw scores S over allowed keys)
 //       * c, one fp32 multiply.
@@ -56,8 +60,10 @@ template <int DH>
 struct Cfg;
 template <>
 struct Cfg<128> {
-    static constexpr int kStagesK = 3;     // K smem stages
-    static constexpr int kStagesV = 2;     // V smem stages
+    static constexpr int kStagesK = 3;     // K smem stages (single CTA)
+    static constexpr int kStagesV = 2;     // V smem stages (single CTA)
+    static constexpr int kStagesKPair = 4; // K half-tile stages (CTA pair)
+    static constexpr int kStagesVPair = 4; // V half-tile stages (CTA pair)
     static constexpr int kChunk = 256;     // keys per chunk (0 = one chunk)
     static constexpr int kOCol = 256;      // TMEM column of the chunk accumulator
     static constexpr int kAccCol = 384;    // TMEM column of the folded accumulator
@@ -66,6 +72,8 @@ template <>
 struct Cfg<256> {
     static constexpr int kStagesK = 1;
     static constexpr int kStagesV = 1;
+    static constexpr int kStagesKPair = 2;
+    static constexpr int kStagesVPair = 2;
     static constexpr int kChunk = 0;
     static constexpr int kOCol = 256;
     static constexpr int kAccCol = -1;
@@ -78,11 +86,24 @@ constexpr int kSmallBytes = 512 /*barriers*/ + 64 /*flags*/ + 2 * 2 * kRows * 4 
 template <int DH>
 constexpr size_t tile_bytes() { return (size_t)(DH / 64) * 16384; }
 
-template <int DH>
+// One K stage: the 128-key tile, or with a CTA pair this CTA's 64 keys (all
+// of the head dim).  One V stage: the 128-key tile, or with a pair this CTA's
+// half of the head dim (all 128 keys).
+template <int DH, bool PAIR>
+constexpr size_t k_stage_bytes() { return PAIR ? tile_bytes<DH>() / 2 : tile_bytes<DH>(); }
+template <int DH, bool PAIR>
+constexpr size_t v_stage_bytes() { return PAIR ? tile_bytes<DH>() / 2 : tile_bytes<DH>(); }
+
+template <int DH, bool PAIR>
+constexpr int stages_k() { return PAIR ? Cfg<DH>::kStagesKPair : Cfg<DH>::kStagesK; }
+template <int DH, bool PAIR>
+constexpr int stages_v() { return PAIR ? Cfg<DH>::kStagesVPair : Cfg<DH>::kStagesV; }
+
+template <int DH, bool PAIR>
 constexpr size_t smem_bytes()
 {
-    return 1024 /*alignment slack*/ + tile_bytes<DH>() * (1 + Cfg<DH>::kStagesK + Cfg<DH>::kStagesV) +
-           kSmallBytes;
+    return 1024 /*alignment slack*/ + tile_bytes<DH>() /*Q*/ + k_stage_bytes<DH, PAIR>() * stages_k<DH, PAIR>() +
+           v_stage_bytes<DH, PAIR>() * stages_v<DH, PAIR>() + kSmallBytes;
 }
 
 // Split-KV partial-state record of one chunk (fp32): m[R], l[R] padded to a
@@ -101,7 +122,7 @@ __host__ __device__ constexpr int64_t part_record_floats(int R, int DH)
 // (fold_coef) runs once per row, then every element applies fold_elem in
 // chunk order -- the same operations, in the same order, as the in-CTA fold.
 template <int DH>
-__device__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int nchunks, int rv,
+__device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int nchunks, int rv,
                                        int64_t tok_first, int kvh, float *work, int work_floats,
                                        int *flag_last)
 {
@@ -180,21 +201,37 @@ __device__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int 
             const bool row_lead = (e % DH) == 0;  // also carries the row's (m, l)
             float oa = s_acc[e];
             float ma = s_run[2 * r], la = s_run[2 * r + 1];
-#pragma unroll 4
-            for (int c = 0; c < cn; ++c) {
-                Fold f;
-                f.sa = s_cf[(c * rv + r) * 2];
-                f.sc = s_cf[(c * rv + r) * 2 + 1];
-                f.mode = s_md[c * rv + r];
-                oa = fold_elem(oa, s_o[c * rv * DH + e], f);
+            for (int cb = 0; cb < cn; cb += 8) {
+                // operands of up to 8 chunks first (independent loads), then the chain
+                float o8[8], sa8[8], sc8[8];
+                int md8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int c = min(cb + k, cn - 1);
+                    o8[k] = s_o[c * rv * DH + e];
+                    sa8[k] = s_cf[(c * rv + r) * 2];
+                    sc8[k] = s_cf[(c * rv + r) * 2 + 1];
+                    md8[k] = (cb + k < cn) ? s_md[c * rv + r] : 0;  // past the end: keep
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    Fold f;
+                    f.sa = sa8[k];
+                    f.sc = sc8[k];
+                    f.mode = md8[k];
+                    oa = fold_elem(oa, o8[k], f);
+                }
                 if (row_lead) {
-                    const float mc = s_ml[(c * rv + r) * 2], lc = s_ml[(c * rv + r) * 2 + 1];
-                    if (f.mode == 1) {
-                        ma = mc;
-                        la = lc;
-                    } else if (f.mode == 2) {
-                        ma = fmaxf(ma, mc);
-                        la = __fadd_rn(__fmul_rn(la, f.sa), __fmul_rn(lc, f.sc));
+                    for (int k = 0; k < 8 && cb + k < cn; ++k) {
+                        const int c = cb + k;
+                        const float mc = s_ml[(c * rv + r) * 2], lc = s_ml[(c * rv + r) * 2 + 1];
+                        if (md8[k] == 1) {
+                            ma = mc;
+                            la = lc;
+                        } else if (md8[k] == 2) {
+                            ma = fmaxf(ma, mc);
+                            la = __fadd_rn(__fmul_rn(la, sa8[k]), __fmul_rn(lc, sc8[k]));
+                        }
                     }
                 }
             }
@@ -330,20 +367,33 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
     return u;
 }
 
-template <int DH>
+// PAIR: the CTAs of a two-CTA cluster take query tiles 2g (rank 0, the
+// leader) and 2g+1 of one (request, KV head) and share every MMA
+// (cta_group::2, M = 256).  Each CTA loads half of each K tile (keys 0-63 in
+// the leader, 64-127 in the other) and half of each V tile (the lower or upper
+// half of the head dim), so a CTA moves half the bytes per score it computes.
+// The leader's thread issues all MMAs; tile-full barriers, P-ready and
+// fold-done barriers live in the leader, stage-release and S/PV-done commits
+// go to both CTAs.  Every row still sees the same operation sequence (C1-C6).
+template <int DH, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = Cfg<DH>;
     constexpr int NKB = DH / 64;                     // 64-column (128-byte) blocks of the head dim
-    constexpr int TILE_BYTES = (int)tile_bytes<DH>();  // 128 rows (or keys) x DH BF16
-    constexpr int NSK = C::kStagesK;
-    constexpr int NSV = C::kStagesV;
+    constexpr int TILE_BYTES = (int)tile_bytes<DH>();  // 128 rows x DH BF16 (the Q tile)
+    constexpr int NSK = stages_k<DH, PAIR>();
+    constexpr int NSV = stages_v<DH, PAIR>();
+    constexpr int KST = (int)k_stage_bytes<DH, PAIR>();
+    constexpr int VST = (int)v_stage_bytes<DH, PAIR>();
+    constexpr int KBLK = PAIR ? 8192 : 16384;        // bytes of one 64-column block of a K stage
+    constexpr int VKB = PAIR ? NKB / 2 : NKB;        // 64-column blocks of a V stage
+    constexpr int CL = PAIR ? 2 : 1;
     constexpr bool CHUNKED = C::kChunk > 0;
     constexpr int CHUNK_DIV = CHUNKED ? C::kChunk : 1;  // divisor used only when CHUNKED
     constexpr int TPC = CHUNKED ? C::kChunk / kKeys : 1;  // tiles per chunk
     constexpr uint32_t ACC_COL = C::kAccCol < 0 ? 0u : (uint32_t)C::kAccCol;
-    constexpr uint32_t ID_QK = idesc_bf16_f32(kRows, kKeys, false);
-    constexpr uint32_t ID_PV = idesc_bf16_f32(kRows, DH, true);
+    constexpr uint32_t ID_QK = idesc_bf16_f32(CL * kRows, kKeys, false);
+    constexpr uint32_t ID_PV = idesc_bf16_f32(CL * kRows, DH, true);
     // barrier slots
     constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
     constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_CR = B_PV + 2;
@@ -356,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;
     uint8_t *sK = sQ + TILE_BYTES;
-    uint8_t *sV = sK + NSK * TILE_BYTES;
-    uint8_t *small = sV + NSV * TILE_BYTES;
+    uint8_t *sV = sK + NSK * KST;
+    uint8_t *small = sV + NSV * VST;
     uint64_t *bars = reinterpret_cast<uint64_t *>(small);
     int *sflags = reinterpret_cast<int *>(small + 512);  // [0] abort [1] tmem [2] last [3] bad
     float *s_x = reinterpret_cast<float *>(small + 512 + 64);   // [2 exchanges][2 halves][128]
@@ -366,10 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     // bounded wait on barrier slot i for the given phase parity
     auto wb = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, abort_flag, p.err, i); };
+    // the same for a barrier that the other CTA of a pair arrives on (acquire at
+    // cluster scope)
+    auto wbc = [&](int i, uint32_t parity) {
+        return PAIR ? wait_bar_cluster(bar(i), parity, abort_flag, p.err, i) : wait_bar(bar(i), parity, abort_flag, p.err, i);
+    };
     const int tid = threadIdx.x;
     const int warp = tid / 32, lane = tid % 32;
     float *const merge_work = reinterpret_cast<float *>(sK);
-    constexpr int kMergeWorkFloats = (NSK + NSV) * TILE_BYTES / 4;
+    constexpr int kMergeWorkFloats = (NSK * KST + NSV * VST) / 4;
 
     // ---------------------------------------------------------- work unit --
     int b, kvh, qt, c_grid = 0;
@@ -384,10 +439,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         c_grid = un.c;
         meta = un.meta;
     } else {
-        // longest work first: later query tiles see more keys
-        const long long u = blockIdx.x;
+        // longest work first: later query tiles see more keys.  With cl = 2
+        // the CTA pair takes query tiles 2g and 2g+1 of one (request, KV head).
+        const long long u = blockIdx.x / CL;
         const long long nbh = (long long)p.num_seqs * p.hkv;
-        qt = p.qtiles - 1 - (int)(u / nbh);
+        const int g = (PAIR ? p.npairs : p.qtiles) - 1 - (int)(u / nbh);
+        qt = PAIR ? 2 * g + (int)cluster_ctarank() : g;
         kvh = (int)((u % nbh) % p.hkv);
         b = (int)((u % nbh) / p.hkv);
         meta = read_meta(p, b);
@@ -395,20 +452,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int qs = meta.qs, qn = meta.qn, L = meta.L;
     const int tok0 = qt * p.tq;
     if (!meta.ok) {
-        if (!p.split && qt == p.qtiles - 1 && tid == 0)
-            record_error(p.err, kErrBadMetadata, b);
-        if (p.split && tid == 0)
+        if (tid == 0 && (p.split || qt == 0))
             record_error(p.err, kErrBadMetadata, b);
         if (meta.sane && tok0 < qn)
             write_nan_rows<DH>(p, (int64_t)qs + tok0, min(p.tq, qn - tok0), kvh);
-        return;
+        return;  // the pair partner (same request) leaves too
     }
-    if (tok0 >= qn)
-        return;
-    const int ntok = min(p.tq, qn - tok0);
+    // A CTA of a pair whose tile lies past the request still runs the shared
+    // K/V pipeline (with no rows of its own) while its partner has work.
+    const int qt_base = PAIR ? (qt & ~1) : qt;
+    if (qt_base * p.tq >= qn)
+        return;  // the whole pair (or the single CTA) has nothing to do
+    const int ntok = max(0, min(p.tq, qn - tok0));
     const int rows_valid = ntok * p.group;
     const int64_t tok_first = (int64_t)qs + tok0;
-    const int kend = L - qn + tok0 + ntok;  // keys [0, kend) are needed by some row
+    // keys [0, kend) are needed by some row of the pair
+    const int last_tok = min(qn, (qt_base + CL) * p.tq);
+    const int kend = L - qn + last_tok;
     const int nchunks = CHUNKED ? (kend + CHUNK_DIV - 1) / CHUNK_DIV : 1;
     int kbeg = 0, kstop = kend;
     if (p.split) {
@@ -434,6 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     int ids_cur = (warp == 0) ? load16(t_begin) : 0;
 
     // -------------------------------------------------------------- setup --
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;  // 0: the pair's leader (MMA issuer)
+    const bool leader = crank == 0;
+    // a barrier slot of the leader CTA as a shared::cluster address
+    auto lead_bar = [&](int i) { return PAIR ? mapa_shared(bar(i), 0) : bar(i); };
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < NSK; ++s) {
@@ -441,16 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             mbar_init(bar(B_KE + s), 1);
         }
         for (int s = 0; s < NSV; ++s) {
-            mbar_init(bar(B_VF + s), 1);
+            // the leader's V-full also takes the other CTA's arrival
+            mbar_init(bar(B_VF + s), PAIR && leader ? 2 : 1);
             mbar_init(bar(B_VE + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_PF + i), 8);
+            mbar_init(bar(B_PF + i), 8 * CL);  // softmax warps of every CTA of the pair
             mbar_init(bar(B_PV + i), 1);
             mbar_init(bar(B_CR + i), 8);
         }
-        mbar_init(bar(B_OF), 4);
+        mbar_init(bar(B_OF), 4 * CL);
         mbar_init(bar(B_PROD), 1);
         mbar_init(bar(B_DONE), 1);
         sflags[0] = 0;
@@ -458,8 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(&sflags[1]), 512);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_addr(&sflags[1]), 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_addr(&sflags[1]), 512);
+            tmem_relinquish();
+        }
     }
     if (tid == 64) {
         prefetch_tensormap(&p.tm_q);
@@ -467,9 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         prefetch_tensormap(&p.tm_v);
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync_all();  // both CTAs' barriers and TMEM exist before either is used
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = static_cast<uint32_t>(sflags[1]);
+    // The key tile is the last one and runs past kend: V rows of keys >= kend
+    // are zeroed after they land (stale or poisoned data).
+    auto zero_tile = [&](int t) { return (t + 1) * kKeys > kend; };
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
@@ -477,12 +553,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         int last_k_use[NSK], last_v_use[NSV];
         for (int s = 0; s < NSK; ++s) last_k_use[s] = -1;
         for (int s = 0; s < NSV; ++s) last_v_use[s] = -1;
-        if (lane == 0)  // Q box: 64 columns x G heads x tq tokens per 64-column block
-            mbar_arrive_expect_tx(bar(B_Q), NKB * 128 * p.group * p.tq);
+        // Q box: 64 columns x G heads x tq tokens per 64-column block; with a
+        // pair both Q tiles are credited to the leader's barrier
+        if (lane == 0 && leader)
+            mbar_arrive_expect_tx(bar(B_Q), CL * NKB * 128 * p.group * p.tq);
         __syncwarp();
-        if (lane < NKB)
-            tma_load_3d(smem_addr(sQ + lane * 16384), &p.tm_q, bar(B_Q), lane * 64, kvh * p.group,
-                        (int)tok_first);
+        if (lane < NKB) {
+            if (PAIR)
+                tma_load_3d_pair(smem_addr(sQ + lane * 16384), &p.tm_q, lead_bar(B_Q), lane * 64, kvh * p.group,
+                                 (int)tok_first);
+            else
+                tma_load_3d(smem_addr(sQ + lane * 16384), &p.tm_q, bar(B_Q), lane * 64, kvh * p.group,
+                            (int)tok_first);
+        }
         // ids of tiles (2j, 2j+1) sit in lanes 0-15 of ids_cur; the next pair is
         // requested one pair ahead
         int ids_next = 0;
@@ -500,39 +583,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (badl)
                 id = 0;  // keep the pipeline flowing; the rows become NaN
             any_bad |= __any_sync(0xffffffffu, badl);
-            const int my_page = lane / NKB, my_kb = lane % NKB;
-            const int my_id = __shfl_sync(0xffffffffu, id, my_page & 7);
-            const bool issue = lane < np * NKB;
+            // K boxes: (page, 64-column block) per lane; a pair member takes the
+            // pages of its 64 keys.  V boxes: all pages, this CTA's blocks.
+            const int k_page = (int)crank * 4 + lane / NKB, k_kb = lane % NKB;
+            const int k_id = __shfl_sync(0xffffffffu, id, k_page & 7);
+            const bool k_issue = lane < (8 / CL) * NKB && k_page < np;
+            const int v_page = lane / VKB, v_kb = lane % VKB;
+            const int v_id = __shfl_sync(0xffffffffu, id, v_page & 7);
+            const bool v_issue = lane < 8 * VKB && v_page < np;
             // K
             const int sk = it % NSK, uk = it / NSK;
             if (lane == 0) {
                 if (uk >= 1)
                     ok = wb(B_KE + sk, (uk - 1) & 1);
-                if (ok)
-                    mbar_arrive_expect_tx(bar(B_KF + sk), np * NKB * 2048);
+                if (ok && leader)
+                    mbar_arrive_expect_tx(bar(B_KF + sk), np * NKB * 2048);  // both halves of the tile
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok)
                 break;
-            if (issue)
-                tma_load_4d(smem_addr(sK + sk * TILE_BYTES + my_kb * 16384 + my_page * 2048), &p.tm_k,
-                            bar(B_KF + sk), my_kb * 64, kvh, 0, my_id);
-            last_k_use[sk] = uk;
+            if (k_issue) {
+                const uint32_t dst = smem_addr(sK + sk * KST + k_kb * KBLK + (k_page - (int)crank * 4) * 2048);
+                if (PAIR)
+                    tma_load_4d_pair(dst, &p.tm_k, lead_bar(B_KF + sk), k_kb * 64, kvh, 0, k_id);
+                else
+                    tma_load_4d(dst, &p.tm_k, bar(B_KF + sk), k_kb * 64, kvh, 0, k_id);
+            }
+            if (!PAIR || leader)
+                last_k_use[sk] = uk;
             // V
             const int sv = it % NSV, uv = it / NSV;
+            // with a pair, the other CTA's last, partly zeroed tile goes through
+            // its own barrier first (relayed by its warp 1 after the zeroing)
+            const bool v_local = PAIR && !leader && zero_tile(t);
             if (lane == 0) {
                 if (uv >= 1)
                     ok = wb(B_VE + sv, (uv - 1) & 1);
-                if (ok)
-                    mbar_arrive_expect_tx(bar(B_VF + sv), np * NKB * 2048);
+                if (ok) {
+                    if (!PAIR)
+                        mbar_arrive_expect_tx(bar(B_VF + sv), np * NKB * 2048);
+                    else if (leader)
+                        mbar_arrive_expect_tx(bar(B_VF + sv), (zero_tile(t) ? 1 : 2) * np * VKB * 2048);
+                    else if (v_local)
+                        mbar_arrive_expect_tx(bar(B_VF + sv), np * VKB * 2048);
+                }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok)
                 break;
-            if (issue)
-                tma_load_4d(smem_addr(sV + sv * TILE_BYTES + my_kb * 16384 + my_page * 2048), &p.tm_v,
-                            bar(B_VF + sv), my_kb * 64, kvh, 0, my_id);
-            last_v_use[sv] = uv;
+            if (v_issue) {
+                const uint32_t dst = smem_addr(sV + sv * VST + v_kb * 16384 + v_page * 2048);
+                const int col = ((int)crank * VKB + v_kb) * 64;
+                if (PAIR)
+                    tma_load_4d_pair(dst, &p.tm_v, v_local ? bar(B_VF + sv) : lead_bar(B_VF + sv), col, kvh, 0,
+                                     v_id);
+                else
+                    tma_load_4d(dst, &p.tm_v, bar(B_VF + sv), col, kvh, 0, v_id);
+            }
+            if (PAIR && !leader && !v_local && lane == 0)
+                mbar_arrive_cluster_relaxed(lead_bar(B_VF + sv));  // a count: the bytes are tracked by the copies
+            if (!PAIR || leader || v_local)
+                last_v_use[sv] = uv;
         }
         if (lane == 0) {
             if (any_bad) {
@@ -547,10 +658,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                         wait_bar_drain(bar(B_KF + s), last_k_use[s] & 1);
                 for (int s = 0; s < NSV; ++s)
                     if (last_v_use[s] >= 0)
-                        wait_bar_drain(bar(B_VF + s), last_v_use[s] & 1);
-                wait_bar_drain(bar(B_Q), 0);
+                        wait_bar_drain(bar(B_VF + s), PAIR && !leader ? 0 : (last_v_use[s] & 1));
+                if (leader)
+                    wait_bar_drain(bar(B_Q), 0);
             }
         }
+        __syncwarp();
+    } else if (warp == 1 && PAIR && !leader) {
+        // ------------------------------------- pair member: V relay only --
+        // Its last tile's V half landed on its own barrier; zero the rows of
+        // keys >= kend, then hand the tile to the leader's V-full barrier.
+        if (n_it > 0 && zero_tile(t_end - 1)) {
+            const int j = n_it - 1, sv = j % NSV, t = t_end - 1;
+            bool okz = __all_sync(0xffffffffu, wb(B_VF + sv, 0));
+            if (okz) {
+                const int row0 = kend - t * kKeys;
+                const int nz = (kKeys - row0) * VKB * 8;
+                uint8_t *vs = sV + sv * VST;
+                for (int idx = lane; idx < nz; idx += 32) {
+                    const int row = row0 + idx / (VKB * 8);
+                    const int rem = idx % (VKB * 8);
+                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * 16384 + row * 128 + (rem % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(lead_bar(B_VF + sv));
+            }
+        }
+        // the leader's MMAs read this CTA's TMEM and shared memory until its
+        // final commit
+        if (lane == 0)
+            wait_bar_drain(bar(B_DONE), 0);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer --
@@ -561,18 +701,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         auto issue_pv = [&](int j) -> bool {
             const int sv = j % NSV;
             const int t = t_begin + j;
-            bool okj = wb(B_VF + sv, (j / NSV) & 1);
+            bool okj = wbc(B_VF + sv, (j / NSV) & 1);
             okj = __all_sync(0xffffffffu, okj);
             if (!okj)
                 return false;
-            if ((t + 1) * kKeys > kend) {
+            if (zero_tile(t)) {
                 // keys >= kend: zero their V rows (stale or poisoned data)
                 const int row0 = kend - t * kKeys;
-                const int nz = (kKeys - row0) * NKB * 8;
-                uint8_t *vs = sV + sv * TILE_BYTES;
+                const int nz = (kKeys - row0) * VKB * 8;
+                uint8_t *vs = sV + sv * VST;
                 for (int idx = lane; idx < nz; idx += 32) {
-                    const int row = row0 + idx / (NKB * 8);
-                    const int rem = idx % (NKB * 8);
+                    const int row = row0 + idx / (VKB * 8);
+                    const int rem = idx % (VKB * 8);
                     *reinterpret_cast<uint4 *>(vs + (rem / 8) * 16384 + row * 128 + (rem % 8) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -580,25 +720,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             }
             __syncwarp();
             if (lane == 0) {
-                okj = wb(B_PF + (j & 1), (j >> 1) & 1);
+                // operands first: P of keys 0-63 sits in columns 0-31 of the S
+                // buffer, keys 64-127 in columns 64-95 (each softmax half writes
+                // its own); V advances 16 keys (2048 bytes) per instruction
+                const uint32_t pcol = tmem + (uint32_t)(j & 1) * kKeys;
+                const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), 16384, 1024);
+                uint32_t ad[8];
+                uint64_t bd[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    ad[i] = pcol + (uint32_t)((i / 4) * 64 + (i % 4) * 8);
+                    bd[i] = vd0 + (uint64_t)((i * 2048) >> 4);
+                }
+                okj = wbc(B_PF + (j & 1), (j >> 1) & 1);
                 const bool chunk_first = CHUNKED ? ((t * kKeys) % CHUNK_DIV == 0) : (j == 0);
                 const int k = CHUNKED ? (t * kKeys - kbeg) / CHUNK_DIV : 0;
                 if (okj && chunk_first && k > 0)
-                    okj = wb(B_OF, (k - 1) & 1);
+                    okj = wbc(B_OF, (k - 1) & 1);
                 if (okj) {
                     tc_fence_after();
-                    // P of keys 0-63 sits in columns 0-31 of the S buffer, keys
-                    // 64-127 in columns 64-95 (each softmax half writes its own)
-                    const uint32_t pcol = tmem + (uint32_t)(j & 1) * kKeys;
-                    const uint32_t vbase = smem_addr(sV + sv * TILE_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        const uint64_t bd = sdesc_sw128(vbase + kk * 2048, 16384, 1024);
-                        const uint32_t acol = pcol + (kk / 4) * 64 + (kk % 4) * 8;
-                        mma_bf16_ts(tmem + C::kOCol, acol, bd, ID_PV, (kk > 0 || !chunk_first) ? 1u : 0u);
+                    mma8_ts<CL>(tmem + C::kOCol, ad, bd, ID_PV, chunk_first ? 0u : 1u);
+                    if (PAIR) {
+                        mma_commit_pair_mc(bar(B_VE + sv), 0x3);
+                        mma_commit_pair_mc(bar(B_PV + (j & 1)), 0x3);
+                    } else {
+                        mma_commit(bar(B_VE + sv));
+                        mma_commit(bar(B_PV + (j & 1)));
                     }
-                    mma_commit(bar(B_VE + sv));
-                    mma_commit(bar(B_PV + (j & 1)));
                 }
             }
             return __shfl_sync(0xffffffffu, okj, 0);
@@ -609,19 +757,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 if (lane == 0) {
                     // S buffer it&1 was last read (as P) by PV(it-2), issued earlier
                     // from this thread, and tcgen05 MMAs from one thread run in order.
+                    // Q and K advance 32 bytes per 16-column step inside a
+                    // 64-column block, a block at a time after every four steps.
+                    const uint64_t qd0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
+                    const uint64_t kd0 = sdesc_sw128(smem_addr(sK + sk * KST), 16, 1024);
                     ok = wb(B_KF + sk, (it / NSK) & 1);
                     if (ok) {
                         tc_fence_after();
-                        const uint32_t qbase = smem_addr(sQ);
-                        const uint32_t kbase = smem_addr(sK + sk * TILE_BYTES);
 #pragma unroll
-                        for (int kk = 0; kk < DH / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                            mma_bf16_ss(tmem + (uint32_t)(it & 1) * kKeys, sdesc_sw128(qbase + off, 16, 1024),
-                                        sdesc_sw128(kbase + off, 16, 1024), ID_QK, kk > 0 ? 1u : 0u);
+                        for (int g8 = 0; g8 < DH / 128; ++g8) {
+                            uint64_t ad[8], bd[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int kk = g8 * 8 + i;
+                                ad[i] = qd0 + (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+                                bd[i] = kd0 + (uint64_t)(((kk / 4) * KBLK + (kk % 4) * 32) >> 4);
+                            }
+                            mma8_ss<CL>(tmem + (uint32_t)(it & 1) * kKeys, ad, bd, ID_QK, g8 > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(B_KE + sk));
-                        mma_commit(bar(B_SF + (it & 1)));
+                        if (PAIR) {
+                            mma_commit_pair_mc(bar(B_KE + sk), 0x3);
+                            mma_commit_pair_mc(bar(B_SF + (it & 1)), 0x3);
+                        } else {
+                            mma_commit(bar(B_KE + sk));
+                            mma_commit(bar(B_SF + (it & 1)));
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -629,9 +789,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (ok && it >= 1)
                 ok = issue_pv(it - 1);
         }
-        // all MMAs retired before TMEM is released
+        // all MMAs retired before TMEM is released (in both CTAs of a pair)
         if (lane == 0) {
-            mma_commit(bar(B_DONE));
+            if (PAIR)
+                mma_commit_pair_mc(bar(B_DONE), 0x3);
+            else
+                mma_commit(bar(B_DONE));
             wait_bar_drain(bar(B_DONE), 0);
         }
         __syncwarp();
@@ -768,7 +931,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(bar(B_PF + sb));
+                // P (and any O rescale) is in this CTA's tensor memory: ordered by
+                // tcgen05.wait::st and the fence above, so a relaxed arrival will do
+                if (PAIR)
+                    mbar_arrive_cluster_relaxed(lead_bar(B_PF + sb));
+                else
+                    mbar_arrive(bar(B_PF + sb));
                 if (chunk_end)
                     mbar_arrive(bar(B_CR + (k & 1)));
             }
@@ -875,16 +1043,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             tc_fence_before();
             __syncwarp();
             if (!final_chunk && lane == 0)
-                mbar_arrive(bar(B_OF));
+            {
+                if (PAIR)
+                    mbar_arrive_cluster_relaxed(lead_bar(B_OF));  // tensor-memory reads only
+                else
+                    mbar_arrive(bar(B_OF));
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync_all();  // both CTAs are done with TMEM, barriers and shared memory
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
-    }
+        if (PAIR)
+            tmem_dealloc_pair(tmem, 512);
+        else
+            tmem_dealloc(tmem, 512);
+    }  // no CTA leaves while its partner may still write into it
     if (p.split)
         split_arrive_and_merge<DH>(p, unit_q, nchunks, rows_valid, tok_first, kvh, merge_work,
                                    kMergeWorkFloats, &sflags[2]);
@@ -920,19 +1099,27 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
         pl.ws_counter_bytes = ((units_q * 4 + 255) / 256) * 256;
         pl.ws_bytes = pl.ws_counter_bytes + units_q * pl.nch * (size_t)part_record_floats(pl.ws_rows, head_dim) * 4;
     }
-    pl.grid = full_ctas * pl.nch * (head_dim == 512 ? 2 : 1);  // head dim 512: a CTA pair per tile
+    // in-CTA schedule with several query tiles: CTA pairs share every MMA
+    // (head dims 128/256)
+    pl.cl = (!pl.split && head_dim != 512 && pl.qtiles >= 2) ? 2 : 1;
+    const long long qgroups = pl.cl == 2 ? (pl.qtiles + 1) / 2 * 2 : pl.qtiles;
+    pl.grid = (long long)num_seqs * num_kv_heads * qgroups * pl.nch * (head_dim == 512 ? 2 : 1);
     *plan = pl;
     return true;
 }
 
+template <int DH, bool PAIR>
+static cudaError_t set_smem_attribute()
+{
+    return cudaFuncSetAttribute(attn_kernel<DH, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<DH, PAIR>());
+}
+
 cudaError_t init_attention_attributes()
 {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_bytes<128>());
-    if (e != cudaSuccess)
-        return e;
-    e = cudaFuncSetAttribute(attn_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<256>());
-    if (e != cudaSuccess)
+    cudaError_t e;
+    if ((e = set_smem_attribute<128, false>()) != cudaSuccess || (e = set_smem_attribute<128, true>()) != cudaSuccess ||
+        (e = set_smem_attribute<256, false>()) != cudaSuccess || (e = set_smem_attribute<256, true>()) != cudaSuccess)
         return e;
     return init_attention512_attributes();
 }
@@ -986,10 +1173,24 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.max_seq_len = a.max_seq_len;
     p.ws_rows = pl.ws_rows;
     p.split = pl.split ? 1 : 0;
+    p.npairs = (pl.qtiles + 1) / 2;
     // C2: scale * log2(e) formed once, in fp32, on the host
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    attn_kernel<DH><<<(unsigned)pl.grid, kThreads, smem_bytes<DH>(), stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.cl == 2 ? smem_bytes<DH, true>() : smem_bytes<DH, false>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pl.cl == 2 ? 1 : 0;
+    if (pl.cl == 2)
+        return cudaLaunchKernelEx(&cfg, attn_kernel<DH, true>, p);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<DH, false>, p);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &pl, ErrState *err, cudaStream_t stream,
@@ -997,7 +1198,9 @@ cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &pl, ErrState *er
 {
     if (info && info_len)
         snprintf(info, info_len, "attention dh=%d schedule=%s grid=%lld qtiles=%d chunks=%d kv_tile=%d chunk=%d",
-                 pl.head_dim, pl.split ? "split-kv" : (pl.head_dim == 512 ? "in-cta-pair" : "in-cta"), pl.grid,
+                 pl.head_dim,
+                 pl.split ? "split-kv" : (pl.head_dim == 512 ? "in-cta-pair" : (pl.cl == 2 ? "in-cta-pair2sm" : "in-cta")),
+                 pl.grid,
                  pl.qtiles, pl.nch, pl.head_dim == 512 ? 64 : kKeys, pl.head_dim == 128 ? Cfg<128>::kChunk : 0);
     if (pl.grid == 0)
         return cudaSuccess;

@@ -44,26 +44,6 @@ constexpr size_t smem_bytes()
 
 }  // namespace d512
 
-// Bounded wait for a phase completed by the peer CTA (acquire at cluster
-// scope).
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                 ErrState *err, int where)
-{
-    if (mbar_try_wait_cluster(bar, parity))
-        return true;
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (*abort_flag)
-            return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            record_error(err, kErrTimeout, ((long long)blockIdx.x << 8) | where);
-            return false;
-        }
-    }
-    return true;
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kernel(const __grid_constant__ AttnParams p)
 {
     using namespace d512;

@@ -36,6 +36,7 @@ struct AttnParams {
     int32_t max_query_len, max_seq_len;
     int32_t ws_rows;
     int32_t split;
+    int32_t npairs;  // query-tile pairs (in-CTA schedule on CTA pairs)
     float scale_log2;
 };
 
@@ -92,6 +93,26 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
         return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            record_error(err, kErrTimeout, ((long long)blockIdx.x << 8) | where);
+            return false;
+        }
+    }
+    return true;
+}
+
+// wait_bar with acquire at cluster scope: the phase may be completed by an
+// arrival from the other CTA of a cluster.
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                 ErrState *err, int where)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_cluster(bar, parity)) {
         if (*abort_flag)
             return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {

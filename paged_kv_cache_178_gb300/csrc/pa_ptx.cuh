@@ -106,17 +106,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (BF16 inputs, FP32 accumulate).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M x 16 BF16 per K-step,
 // row = TMEM lane, two consecutive K elements per 32-bit column (element 2i
 // in the low half).
@@ -232,6 +221,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
                  : "memory");
 }
 
+// Arrive on an mbarrier of another CTA in the cluster without ordering this
+// thread's memory writes (relaxed).  For hand-offs of tensor memory, whose
+// order is given by tcgen05.wait + tcgen05.fence::before_thread_sync, and of
+// pure counts.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // Wait with acquire at cluster scope (the phase was completed by a peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
@@ -258,6 +256,114 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
                  "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
                  "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+// ---------------------------------------------- eight-MMA groups (K = 128) --
+// One K = 128 product as eight kind::f16 instructions issued back to back from
+// a single asm block, descriptors computed beforehand: nothing is scheduled
+// between the MMAs.  Instruction i accumulates onto D when i > 0 or
+// `accumulate` is set.  CG is the cta_group (1, or 2 for a CTA pair).
+#define PA_MMA8_BODY(CG, AFORM)                                                                          \
+    "{\n\t.reg .pred p0, p1;\n\t"                                                                         \
+    "setp.ne.b32 p0, %18, 0;\n\t"                                                                         \
+    "setp.ne.b32 p1, 1, 0;\n\t"                                                                           \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(1) ", %9, %17, p0;\n\t"                       \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(2) ", %10, %17, p1;\n\t"                      \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(3) ", %11, %17, p1;\n\t"                      \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(4) ", %12, %17, p1;\n\t"                      \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(5) ", %13, %17, p1;\n\t"                      \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(6) ", %14, %17, p1;\n\t"                      \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(7) ", %15, %17, p1;\n\t"                      \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], " AFORM(8) ", %16, %17, p1;\n\t}"
+#define PA_A_SMEM(i) "%" #i
+#define PA_A_TMEM(i) "[%" #i "]"
+
+template <int CG>
+__device__ __forceinline__ void mma8_ss(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                        uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (CG == 1)
+        asm volatile(PA_MMA8_BODY(1, PA_A_SMEM)::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]),
+                     "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
+                     "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile(PA_MMA8_BODY(2, PA_A_SMEM)::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]),
+                     "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
+                     "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+                     : "memory");
+}
+
+// A from tensor memory: a[i] is the TMEM address of instruction i's A slice.
+template <int CG>
+__device__ __forceinline__ void mma8_ts(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                        uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (CG == 1)
+        asm volatile(PA_MMA8_BODY(1, PA_A_TMEM)::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
+                     "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
+                     "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile(PA_MMA8_BODY(2, PA_A_TMEM)::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
+                     "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
+                     "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+                     : "memory");
+}
+
+// ------------------------------------------------- CTA pairs (cta_group::2) --
+// A kernel uses one cta_group value for all of its tcgen05 instructions; the
+// pair variants below serve kernels where an even/odd CTA pair of a cluster
+// shares each MMA (M = 256: rows 0-127 in the even CTA's TMEM, 128-255 in
+// the odd one's; the B operand's N columns split in halves between the two
+// CTAs' shared memory at the same offset).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// Completion of this thread's pair MMAs arrives on `bar`'s offset in every
+// CTA of `mask`.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"(mask)
+                 : "memory");
+}
+
+// TMA tile loads into this CTA's shared memory whose byte count is credited to
+// an mbarrier that may sit in the peer CTA of the pair (`bar` is a
+// shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                  : "memory");
 }
 
