@@ -194,52 +194,53 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
             s_md[c * rv + r] = f.mode;
         }
         __syncthreads();
-        // (c) the sequential parts, in chunk order: O per element, (m, l) per
-        //     row -- the same operations fold_coef / fold_elem perform
-        for (int e = tid; e < rv * DH; e += nth) {
-            const int r = e / DH;
-            const bool row_lead = (e % DH) == 0;  // also carries the row's (m, l)
-            float oa = s_acc[e];
+        // (c) the sequential parts, in chunk order -- the same operations
+        //     fold_coef / fold_elem perform: (m, l) per row on its own thread,
+        //     O per element, with no branch inside the element chain
+        // (loads first, selects after: only the arithmetic is serial)
+        for (int r = tid; r < rv; r += nth) {
             float ma = s_run[2 * r], la = s_run[2 * r + 1];
-            for (int cb = 0; cb < cn; cb += 8) {
-                // operands of up to 8 chunks first (independent loads), then the chain
-                float o8[8], sa8[8], sc8[8];
-                int md8[8];
+#pragma unroll 4
+            for (int c = 0; c < cn; ++c) {
+                const int md = s_md[c * rv + r];
+                const float2 ml = *reinterpret_cast<const float2 *>(s_ml + (c * rv + r) * 2);
+                const float2 cf = *reinterpret_cast<const float2 *>(s_cf + (c * rv + r) * 2);
+                const float l2 = __fadd_rn(__fmul_rn(la, cf.x), __fmul_rn(ml.y, cf.y));
+                const float m2 = fmaxf(ma, ml.x);
+                la = md == 1 ? ml.y : (md == 2 ? l2 : la);
+                ma = md == 1 ? ml.x : (md == 2 ? m2 : ma);
+            }
+            s_run2[2 * r] = ma;
+            s_run2[2 * r + 1] = la;
+        }
+        // four consecutive elements of one row per thread: one 16-byte load
+        // per chunk, the row's coefficients shared; operands of seven chunks
+        // are loaded before their seven fold steps
+        for (int e4 = tid; e4 < rv * DH / 4; e4 += nth) {
+            const int e = e4 * 4, r = e / DH;
+            float4 oa = *reinterpret_cast<const float4 *>(s_acc + e);
+            for (int cb = 0; cb < cn; cb += 7) {
+                float4 o7[7];
+                float a7[7], b7[7];
+                int m7[7];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < 7; ++k) {
                     const int c = min(cb + k, cn - 1);
-                    o8[k] = s_o[c * rv * DH + e];
-                    sa8[k] = s_cf[(c * rv + r) * 2];
-                    sc8[k] = s_cf[(c * rv + r) * 2 + 1];
-                    md8[k] = (cb + k < cn) ? s_md[c * rv + r] : 0;  // past the end: keep
+                    o7[k] = *reinterpret_cast<const float4 *>(s_o + c * rv * DH + e);
+                    const float2 cf = *reinterpret_cast<const float2 *>(s_cf + (c * rv + r) * 2);
+                    a7[k] = cf.x;
+                    b7[k] = cf.y;
+                    m7[k] = cb + k < cn ? s_md[c * rv + r] : 0;  // past the last chunk: keep
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    Fold f;
-                    f.sa = sa8[k];
-                    f.sc = sc8[k];
-                    f.mode = md8[k];
-                    oa = fold_elem(oa, o8[k], f);
-                }
-                if (row_lead) {
-                    for (int k = 0; k < 8 && cb + k < cn; ++k) {
-                        const int c = cb + k;
-                        const float mc = s_ml[(c * rv + r) * 2], lc = s_ml[(c * rv + r) * 2 + 1];
-                        if (md8[k] == 1) {
-                            ma = mc;
-                            la = lc;
-                        } else if (md8[k] == 2) {
-                            ma = fmaxf(ma, mc);
-                            la = __fadd_rn(__fmul_rn(la, sa8[k]), __fmul_rn(lc, sc8[k]));
-                        }
-                    }
+                for (int k = 0; k < 7; ++k) {
+                    oa.x = fold_elem_sel(oa.x, o7[k].x, a7[k], b7[k], m7[k]);
+                    oa.y = fold_elem_sel(oa.y, o7[k].y, a7[k], b7[k], m7[k]);
+                    oa.z = fold_elem_sel(oa.z, o7[k].z, a7[k], b7[k], m7[k]);
+                    oa.w = fold_elem_sel(oa.w, o7[k].w, a7[k], b7[k], m7[k]);
                 }
             }
-            s_acc[e] = oa;
-            if (row_lead) {
-                s_run2[2 * r] = ma;
-                s_run2[2 * r + 1] = la;
-            }
+            *reinterpret_cast<float4 *>(s_acc + e) = oa;
         }
         __syncthreads();
         for (int r = tid; r < rv; r += nth) {

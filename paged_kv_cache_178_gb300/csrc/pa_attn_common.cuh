@@ -77,6 +77,24 @@ __device__ __forceinline__ float fold_elem(float oa, float oc, const Fold &f)
     return f.mode == 0 ? oa : (f.mode == 1 ? oc : __fadd_rn(__fmul_rn(oa, f.sa), __fmul_rn(oc, f.sc)));
 }
 
+// fold_elem with the mode picked by predicated selects (no branch): the
+// same three candidate results, the same one chosen, bit for bit.
+__device__ __forceinline__ float fold_elem_sel(float oa, float oc, float sa, float sc, int mode)
+{
+    float r;
+    asm("{\n\t.reg .pred p1, p2;\n\t.reg .f32 t1, t2, t3, t4;\n\t"
+        "mul.rn.f32 t1, %1, %3;\n\t"
+        "mul.rn.f32 t2, %2, %4;\n\t"
+        "add.rn.f32 t3, t1, t2;\n\t"
+        "setp.eq.s32 p1, %5, 1;\n\t"
+        "selp.f32 t4, %2, %1, p1;\n\t"
+        "setp.eq.s32 p2, %5, 2;\n\t"
+        "selp.f32 %0, t3, t4, p2;\n\t}"
+        : "=f"(r)
+        : "f"(oa), "f"(oc), "f"(sa), "f"(sc), "r"(mode));
+    return r;
+}
+
 __device__ __forceinline__ float lse_of(float m, float l)
 {
     return __fmul_rn(__fadd_rn(m, __log2f(l)), kLn2);
