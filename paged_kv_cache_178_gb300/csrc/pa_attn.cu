@@ -62,11 +62,11 @@ template <>
 struct Cfg<128> {
     static constexpr int kStagesK = 3;     // K smem stages (single CTA)
     static constexpr int kStagesV = 2;     // V smem stages (single CTA)
-    static constexpr int kStagesKPair = 4; // K half-tile stages (CTA pair)
-    static constexpr int kStagesVPair = 4; // V half-tile stages (CTA pair)
+    static constexpr int kStagesKPair = 3; // K half-tile stages (CTA pair)
+    static constexpr int kStagesVPair = 3; // V half-tile stages (CTA pair)
     static constexpr int kChunk = 256;     // keys per chunk (0 = one chunk)
     static constexpr int kOCol = 256;      // TMEM column of the chunk accumulator
-    static constexpr int kAccCol = 384;    // TMEM column of the folded accumulator
+    static constexpr int kAccCol = 384;    // TMEM column of the folded accumulator (single CTA)
 };
 template <>
 struct Cfg<256> {
@@ -99,11 +99,20 @@ constexpr int stages_k() { return PAIR ? Cfg<DH>::kStagesKPair : Cfg<DH>::kStage
 template <int DH, bool PAIR>
 constexpr int stages_v() { return PAIR ? Cfg<DH>::kStagesVPair : Cfg<DH>::kStagesV; }
 
+// CTA pairs with chunked heads keep two chunk accumulators in TMEM (columns
+// kOCol and kOCol + 128, by chunk parity) so the next chunk's P.V never waits
+// for the fold of the previous one; the folded accumulator then lives in
+// shared memory (fp32, 128 rows).
+template <int DH, bool PAIR>
+constexpr bool acc_in_smem() { return PAIR && Cfg<DH>::kChunk > 0; }
+template <int DH, bool PAIR>
+constexpr size_t acc_smem_bytes() { return acc_in_smem<DH, PAIR>() ? (size_t)kRows * DH * 4 : 0; }
+
 template <int DH, bool PAIR>
 constexpr size_t smem_bytes()
 {
     return 1024 /*alignment slack*/ + tile_bytes<DH>() /*Q*/ + k_stage_bytes<DH, PAIR>() * stages_k<DH, PAIR>() +
-           v_stage_bytes<DH, PAIR>() * stages_v<DH, PAIR>() + kSmallBytes;
+           v_stage_bytes<DH, PAIR>() * stages_v<DH, PAIR>() + acc_smem_bytes<DH, PAIR>() + kSmallBytes;
 }
 
 // Split-KV partial-state record of one chunk (fp32): m[R], l[R] padded to a
@@ -112,6 +121,33 @@ __host__ __device__ constexpr int64_t part_header_floats(int R) { return (2 * R 
 __host__ __device__ constexpr int64_t part_record_floats(int R, int DH)
 {
     return part_header_floats(R) + (int64_t)R * DH;
+}
+
+// Row r of the shared-memory accumulator, columns 32g .. 32g+31, as 32-bit
+// words: 16-byte chunk c of a row sits at chunk (c ^ (r & 7)), so the eight
+// rows of a quarter warp hit eight different bank groups.
+template <int DH>
+__device__ __forceinline__ void acc_row_load(const float4 *acc, int r, int g, uint32_t (&v)[32])
+{
+    const float4 *row = acc + (size_t)r * (DH / 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = row[(g * 8 + i) ^ (r & 7)];
+        v[4 * i] = __float_as_uint(x.x);
+        v[4 * i + 1] = __float_as_uint(x.y);
+        v[4 * i + 2] = __float_as_uint(x.z);
+        v[4 * i + 3] = __float_as_uint(x.w);
+    }
+}
+
+template <int DH>
+__device__ __forceinline__ void acc_row_store(float4 *acc, int r, int g, const uint32_t (&v)[32])
+{
+    float4 *row = acc + (size_t)r * (DH / 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        row[(g * 8 + i) ^ (r & 7)] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
 }
 
 // Arrival on the (request, KV head, query tile) counter; the last CTA to
@@ -393,12 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     constexpr int CHUNK_DIV = CHUNKED ? C::kChunk : 1;  // divisor used only when CHUNKED
     constexpr int TPC = CHUNKED ? C::kChunk / kKeys : 1;  // tiles per chunk
     constexpr uint32_t ACC_COL = C::kAccCol < 0 ? 0u : (uint32_t)C::kAccCol;
+    constexpr bool OBUF2 = acc_in_smem<DH, PAIR>();  // two chunk accumulators, folded one in smem
+    // TMEM column of chunk k's accumulator
+    auto ocol = [](int k) { return (uint32_t)C::kOCol + (OBUF2 ? (uint32_t)(k & 1) * 128u : 0u); };
     constexpr uint32_t ID_QK = idesc_bf16_f32(CL * kRows, kKeys, false);
     constexpr uint32_t ID_PV = idesc_bf16_f32(CL * kRows, DH, true);
     // barrier slots
     constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
     constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_CR = B_PV + 2;
-    constexpr int B_OF = B_CR + 2, B_PROD = B_OF + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
+    constexpr int B_OF = B_CR + 2, B_PROD = B_OF + (OBUF2 ? 2 : 1), B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
     extern __shared__ uint8_t smem_raw[];
@@ -408,7 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     uint8_t *sQ = smem;
     uint8_t *sK = sQ + TILE_BYTES;
     uint8_t *sV = sK + NSK * KST;
-    uint8_t *small = sV + NSV * VST;
+    float4 *sAcc = reinterpret_cast<float4 *>(sV + NSV * VST);  // [128 rows][DH/4], 16-byte chunks XOR-swizzled
+    uint8_t *small = sV + NSV * VST + acc_smem_bytes<DH, PAIR>();
     uint64_t *bars = reinterpret_cast<uint64_t *>(small);
     int *sflags = reinterpret_cast<int *>(small + 512);  // [0] abort [1] tmem [2] last [3] bad
     float *s_x = reinterpret_cast<float *>(small + 512 + 64);   // [2 exchanges][2 halves][128]
@@ -517,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             mbar_init(bar(B_CR + i), 8);
         }
         mbar_init(bar(B_OF), 4 * CL);
+        if (OBUF2)
+            mbar_init(bar(B_OF + 1), 4 * CL);
         mbar_init(bar(B_PROD), 1);
         mbar_init(bar(B_DONE), 1);
         sflags[0] = 0;
@@ -695,11 +737,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer --
+        // With two or more V stages, PV(j) and QK(j+2) are issued back to back
+        // (K(j+2) is waited for first), so the tensor pipe goes from one group
+        // to the next without idling.  QK(j+2) overwrites the S buffer that
+        // PV(j) reads P from: tcgen05 MMAs from one thread run in order.  With
+        // one V stage, K(j+2) is loaded only after PV(j) has released V, so
+        // the order is QK(j+1), PV(j).
+        constexpr bool LOOKAHEAD = NSV >= 2;
         bool ok = true;
         if (lane == 0)
             ok = wb(B_Q, 0);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        auto issue_pv = [&](int j) -> bool {
+        // QK(it), K(it) already resident: Q and K advance 32 bytes per
+        // 16-column step inside a 64-column block, a block after four steps
+        auto issue_qk = [&](int it) {
+            const int sk = it % NSK;
+            const uint64_t qd0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
+            const uint64_t kd0 = sdesc_sw128(smem_addr(sK + sk * KST), 16, 1024);
+            tc_fence_after();
+#pragma unroll
+            for (int g8 = 0; g8 < DH / 128; ++g8) {
+                uint64_t ad[8], bd[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int kk = g8 * 8 + i;
+                    ad[i] = qd0 + (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+                    bd[i] = kd0 + (uint64_t)(((kk / 4) * KBLK + (kk % 4) * 32) >> 4);
+                }
+                mma8_ss<CL>(tmem + (uint32_t)(it & 1) * kKeys, ad, bd, ID_QK, g8 > 0 ? 1u : 0u);
+            }
+            if (PAIR) {
+                mma_commit_pair_mc(bar(B_KE + sk), 0x3);
+                mma_commit_pair_mc(bar(B_SF + (it & 1)), 0x3);
+            } else {
+                mma_commit(bar(B_KE + sk));
+                mma_commit(bar(B_SF + (it & 1)));
+            }
+        };
+        auto wait_kf = [&](int it) { return wb(B_KF + it % NSK, (it / NSK) & 1); };
+        // PV(j) and, when given (qk_next >= 0), QK(qk_next) right behind it
+        auto issue_pv = [&](int j, int qk_next) -> bool {
             const int sv = j % NSV;
             const int t = t_begin + j;
             bool okj = wbc(B_VF + sv, (j / NSV) & 1);
@@ -736,11 +813,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 okj = wbc(B_PF + (j & 1), (j >> 1) & 1);
                 const bool chunk_first = CHUNKED ? ((t * kKeys) % CHUNK_DIV == 0) : (j == 0);
                 const int k = CHUNKED ? (t * kKeys - kbeg) / CHUNK_DIV : 0;
-                if (okj && chunk_first && k > 0)
+                if (OBUF2) {
+                    // the buffer was last read by the fold of chunk k - 2
+                    if (okj && chunk_first && k >= 2)
+                        okj = wbc(B_OF + (k & 1), ((k >> 1) - 1) & 1);
+                } else if (okj && chunk_first && k > 0) {
                     okj = wbc(B_OF, (k - 1) & 1);
+                }
+                if (okj && qk_next >= 0)
+                    okj = wait_kf(qk_next);
                 if (okj) {
                     tc_fence_after();
-                    mma8_ts<CL>(tmem + C::kOCol, ad, bd, ID_PV, chunk_first ? 0u : 1u);
+                    mma8_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
                     if (PAIR) {
                         mma_commit_pair_mc(bar(B_VE + sv), 0x3);
                         mma_commit_pair_mc(bar(B_PV + (j & 1)), 0x3);
@@ -748,47 +832,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                         mma_commit(bar(B_VE + sv));
                         mma_commit(bar(B_PV + (j & 1)));
                     }
+                    if (qk_next >= 0)
+                        issue_qk(qk_next);
                 }
             }
             return __shfl_sync(0xffffffffu, okj, 0);
         };
-        for (int it = 0; ok && it <= n_it; ++it) {
-            if (it < n_it) {
-                const int sk = it % NSK;
-                if (lane == 0) {
-                    // S buffer it&1 was last read (as P) by PV(it-2), issued earlier
-                    // from this thread, and tcgen05 MMAs from one thread run in order.
-                    // Q and K advance 32 bytes per 16-column step inside a
-                    // 64-column block, a block at a time after every four steps.
-                    const uint64_t qd0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
-                    const uint64_t kd0 = sdesc_sw128(smem_addr(sK + sk * KST), 16, 1024);
-                    ok = wb(B_KF + sk, (it / NSK) & 1);
-                    if (ok) {
-                        tc_fence_after();
-#pragma unroll
-                        for (int g8 = 0; g8 < DH / 128; ++g8) {
-                            uint64_t ad[8], bd[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int kk = g8 * 8 + i;
-                                ad[i] = qd0 + (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
-                                bd[i] = kd0 + (uint64_t)(((kk / 4) * KBLK + (kk % 4) * 32) >> 4);
-                            }
-                            mma8_ss<CL>(tmem + (uint32_t)(it & 1) * kKeys, ad, bd, ID_QK, g8 > 0 ? 1u : 0u);
-                        }
-                        if (PAIR) {
-                            mma_commit_pair_mc(bar(B_KE + sk), 0x3);
-                            mma_commit_pair_mc(bar(B_SF + (it & 1)), 0x3);
-                        } else {
-                            mma_commit(bar(B_KE + sk));
-                            mma_commit(bar(B_SF + (it & 1)));
-                        }
-                    }
+        if (LOOKAHEAD) {
+            if (lane == 0)
+                for (int it = 0; ok && it < min(2, n_it); ++it) {
+                    ok = wait_kf(it);
+                    if (ok)
+                        issue_qk(it);
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            for (int j = 0; ok && j < n_it; ++j)
+                ok = issue_pv(j, j + 2 < n_it ? j + 2 : -1);
+        } else {
+            for (int it = 0; ok && it <= n_it; ++it) {
+                if (it < n_it) {
+                    if (lane == 0) {
+                        ok = wait_kf(it);
+                        if (ok)
+                            issue_qk(it);
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                }
+                if (ok && it >= 1)
+                    ok = issue_pv(it - 1, -1);
             }
-            if (ok && it >= 1)
-                ok = issue_pv(it - 1);
         }
         // all MMAs retired before TMEM is released (in both CTAs of a pair)
         if (lane == 0) {
@@ -912,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll 1
                 for (int g = 0; g < DH / 64; ++g) {
                     uint32_t v[32];
-                    const uint32_t col = tmem + lane_off + C::kOCol + (DH / 2) * h + g * 32;
+                    const uint32_t col = tmem + lane_off + ocol(CHUNKED ? it / TPC : 0) + (DH / 2) * h + g * 32;
                     tmem_ld32(col, v);
                     tmem_wait_ld();
 #pragma unroll
@@ -1003,9 +1075,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll 1
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t vc[32], va[32];
-                    tmem_ld32(tmem + lane_off + C::kOCol + g * 32, vc);
-                    if (acc_live)
+                    tmem_ld32(tmem + lane_off + ocol(k) + g * 32, vc);
+                    if (acc_live && !OBUF2)
                         tmem_ld32(tmem + lane_off + ACC_COL + g * 32, va);
+                    if (acc_live && OBUF2)
+                        acc_row_load<DH>(sAcc, r, g, va);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -1019,36 +1093,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 if (row_valid && p.lse)
                     p.lse[tok * p.hq + head] = bad ? __int_as_float(0x7FC00000) : lse_of(f.m, f.l);
             } else {
-                // fold this chunk into the running accumulator (TMEM)
+                // fold this chunk into the running accumulator (TMEM, or shared
+                // memory when the chunk accumulators are double-buffered)
                 const Fold f = fold_coef(m_acc, l_acc, m, l);
                 const bool acc_live = nfold > 0;  // uniform: tcgen05.ld is warp-collective
 #pragma unroll 1
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t vc[32], va[32];
-                    tmem_ld32(tmem + lane_off + C::kOCol + g * 32, vc);
-                    if (acc_live)
+                    tmem_ld32(tmem + lane_off + ocol(k) + g * 32, vc);
+                    if (acc_live && !OBUF2)
                         tmem_ld32(tmem + lane_off + ACC_COL + g * 32, va);
+                    if (acc_live && OBUF2)
+                        acc_row_load<DH>(sAcc, r, g, va);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const float oa = acc_live ? __uint_as_float(va[i]) : 0.f;
                         va[i] = __float_as_uint(fold_elem(oa, __uint_as_float(vc[i]), f));
                     }
-                    tmem_st32(tmem + lane_off + ACC_COL + g * 32, va);
+                    if (OBUF2)
+                        acc_row_store<DH>(sAcc, r, g, va);
+                    else
+                        tmem_st32(tmem + lane_off + ACC_COL + g * 32, va);
                 }
-                tmem_wait_st();
+                if (!OBUF2)
+                    tmem_wait_st();
                 m_acc = f.m;
                 l_acc = f.l;
                 ++nfold;
             }
             tc_fence_before();
             __syncwarp();
-            if (!final_chunk && lane == 0)
-            {
+            if (!final_chunk && lane == 0) {
+                // chunk k's accumulator may be overwritten (tensor-memory reads only)
+                const int of = B_OF + (OBUF2 ? (k & 1) : 0);
                 if (PAIR)
-                    mbar_arrive_cluster_relaxed(lead_bar(B_OF));  // tensor-memory reads only
+                    mbar_arrive_cluster_relaxed(lead_bar(of));
                 else
-                    mbar_arrive(bar(B_OF));
+                    mbar_arrive(bar(of));
             }
         }
     }
