@@ -437,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // barrier slots
     constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
     constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_CR = B_PV + 2;
-    constexpr int B_OF = B_CR + 2, B_PROD = B_OF + (OBUF2 ? 2 : 1), B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
+    constexpr int B_OF = B_CR + 2, B_PROD = B_OF + (OBUF2 ? 2 : 1), B_DONE = B_PROD + 1, B_VZ = B_DONE + 1;
+    constexpr int NBARS = B_VZ + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
     extern __shared__ uint8_t smem_raw[];
@@ -561,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             mbar_init(bar(B_OF + 1), 4 * CL);
         mbar_init(bar(B_PROD), 1);
         mbar_init(bar(B_DONE), 1);
+        mbar_init(bar(B_VZ), 1);
         sflags[0] = 0;
         sflags[3] = 0;
         fence_barrier_init();
@@ -688,6 +690,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (!PAIR || leader || v_local)
                 last_v_use[sv] = uv;
         }
+        // The last tile's V rows of keys >= kend hold stale or poisoned data:
+        // zero them once the tile has landed (the barrier is in that tile's
+        // phase now: the producer starts no later phase), then release the
+        // MMA issuer.  A pair's other CTA zeroes its half in its relay warp.
+        if (ok && n_it > 0 && zero_tile(t_end - 1) && (!PAIR || leader)) {
+            const int j = n_it - 1, sv = j % NSV, t = t_end - 1;
+            const bool okz = __all_sync(0xffffffffu, wbc(B_VF + sv, (j / NSV) & 1));
+            if (okz) {
+                const int row0 = kend - t * kKeys;
+                const int nz = (kKeys - row0) * VKB * 8;
+                uint8_t *vs = sV + sv * VST;
+                for (int idx = lane; idx < nz; idx += 32) {
+                    const int row = row0 + idx / (VKB * 8);
+                    const int rem = idx % (VKB * 8);
+                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * 16384 + row * 128 + (rem % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(B_VZ));
+            }
+        }
         if (lane == 0) {
             if (any_bad) {
                 record_error(p.err, kErrBadMetadata, b);
@@ -775,93 +800,79 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             }
         };
         auto wait_kf = [&](int it) { return wb(B_KF + it % NSK, (it / NSK) & 1); };
-        // PV(j) and, when given (qk_next >= 0), QK(qk_next) right behind it
+        // PV(j) and, when given (qk_next >= 0), QK(qk_next) right behind it.
+        // Lane 0 alone: no warp-wide step between MMA groups.
         auto issue_pv = [&](int j, int qk_next) -> bool {
             const int sv = j % NSV;
             const int t = t_begin + j;
-            bool okj = wbc(B_VF + sv, (j / NSV) & 1);
-            okj = __all_sync(0xffffffffu, okj);
-            if (!okj)
-                return false;
-            if (zero_tile(t)) {
-                // keys >= kend: zero their V rows (stale or poisoned data)
-                const int row0 = kend - t * kKeys;
-                const int nz = (kKeys - row0) * VKB * 8;
-                uint8_t *vs = sV + sv * VST;
-                for (int idx = lane; idx < nz; idx += 32) {
-                    const int row = row0 + idx / (VKB * 8);
-                    const int rem = idx % (VKB * 8);
-                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * 16384 + row * 128 + (rem % 8) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (lane == 0) {
-                // operands first: P of keys 0-63 sits in columns 0-31 of the S
-                // buffer, keys 64-127 in columns 64-95 (each softmax half writes
-                // its own); V advances 16 keys (2048 bytes) per instruction
-                const uint32_t pcol = tmem + (uint32_t)(j & 1) * kKeys;
-                const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), 16384, 1024);
-                uint32_t ad[8];
-                uint64_t bd[8];
+            // operands first: P of keys 0-63 sits in columns 0-31 of the S
+            // buffer, keys 64-127 in columns 64-95 (each softmax half writes
+            // its own); V advances 16 keys (2048 bytes) per instruction
+            const uint32_t pcol = tmem + (uint32_t)(j & 1) * kKeys;
+            const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), 16384, 1024);
+            uint32_t ad[8];
+            uint64_t bd[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    ad[i] = pcol + (uint32_t)((i / 4) * 64 + (i % 4) * 8);
-                    bd[i] = vd0 + (uint64_t)((i * 2048) >> 4);
-                }
-                okj = wbc(B_PF + (j & 1), (j >> 1) & 1);
-                const bool chunk_first = CHUNKED ? ((t * kKeys) % CHUNK_DIV == 0) : (j == 0);
-                const int k = CHUNKED ? (t * kKeys - kbeg) / CHUNK_DIV : 0;
-                if (OBUF2) {
-                    // the buffer was last read by the fold of chunk k - 2
-                    if (okj && chunk_first && k >= 2)
-                        okj = wbc(B_OF + (k & 1), ((k >> 1) - 1) & 1);
-                } else if (okj && chunk_first && k > 0) {
-                    okj = wbc(B_OF, (k - 1) & 1);
-                }
-                if (okj && qk_next >= 0)
-                    okj = wait_kf(qk_next);
-                if (okj) {
-                    tc_fence_after();
-                    mma8_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
-                    if (PAIR) {
-                        mma_commit_pair_mc(bar(B_VE + sv), 0x3);
-                        mma_commit_pair_mc(bar(B_PV + (j & 1)), 0x3);
-                    } else {
-                        mma_commit(bar(B_VE + sv));
-                        mma_commit(bar(B_PV + (j & 1)));
-                    }
-                    if (qk_next >= 0)
-                        issue_qk(qk_next);
-                }
+            for (int i = 0; i < 8; ++i) {
+                ad[i] = pcol + (uint32_t)((i / 4) * 64 + (i % 4) * 8);
+                bd[i] = vd0 + (uint64_t)((i * 2048) >> 4);
             }
-            return __shfl_sync(0xffffffffu, okj, 0);
+            const bool chunk_first = CHUNKED ? ((t * kKeys) % CHUNK_DIV == 0) : (j == 0);
+            const int k = CHUNKED ? (t * kKeys - kbeg) / CHUNK_DIV : 0;
+            // The last tile's V rows of keys >= kend are zeroed by the producer
+            // first (generic writes, possibly relayed from the pair's other
+            // CTA: acquire at cluster scope).  V-full (copies and a relaxed
+            // count), P-ready and fold-done hand over tensor memory or TMA
+            // data only: CTA-scope waits suffice.
+            bool okj = zero_tile(t) ? wbc(B_VZ, 0) : wb(B_VF + sv, (j / NSV) & 1);
+            if (okj)
+                okj = wb(B_PF + (j & 1), (j >> 1) & 1);
+            if (OBUF2) {
+                // the buffer was last read by the fold of chunk k - 2
+                if (okj && chunk_first && k >= 2)
+                    okj = wb(B_OF + (k & 1), ((k >> 1) - 1) & 1);
+            } else if (okj && chunk_first && k > 0) {
+                okj = wb(B_OF, (k - 1) & 1);
+            }
+            if (okj && qk_next >= 0)
+                okj = wait_kf(qk_next);
+            if (okj) {
+                tc_fence_after();
+                mma8_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
+                if (PAIR) {
+                    mma_commit_pair_mc(bar(B_VE + sv), 0x3);
+                    mma_commit_pair_mc(bar(B_PV + (j & 1)), 0x3);
+                } else {
+                    mma_commit(bar(B_VE + sv));
+                    mma_commit(bar(B_PV + (j & 1)));
+                }
+                if (qk_next >= 0)
+                    issue_qk(qk_next);
+            }
+            return okj;
         };
-        if (LOOKAHEAD) {
-            if (lane == 0)
+        if (lane == 0) {
+            if (LOOKAHEAD) {
                 for (int it = 0; ok && it < min(2, n_it); ++it) {
                     ok = wait_kf(it);
                     if (ok)
                         issue_qk(it);
                 }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            for (int j = 0; ok && j < n_it; ++j)
-                ok = issue_pv(j, j + 2 < n_it ? j + 2 : -1);
-        } else {
-            for (int it = 0; ok && it <= n_it; ++it) {
-                if (it < n_it) {
-                    if (lane == 0) {
+                for (int j = 0; ok && j < n_it; ++j)
+                    ok = issue_pv(j, j + 2 < n_it ? j + 2 : -1);
+            } else {
+                for (int it = 0; ok && it <= n_it; ++it) {
+                    if (it < n_it) {
                         ok = wait_kf(it);
                         if (ok)
                             issue_qk(it);
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok && it >= 1)
+                        ok = issue_pv(it - 1, -1);
                 }
-                if (ok && it >= 1)
-                    ok = issue_pv(it - 1, -1);
             }
         }
+        __syncwarp();
         // all MMAs retired before TMEM is released (in both CTAs of a pair)
         if (lane == 0) {
             if (PAIR)
