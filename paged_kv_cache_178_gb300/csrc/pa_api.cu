@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots, int64_t block_stride,
     int64_t token_stride, int64_t head_stride, const int64_t *__restrict__ slot_mapping, ErrState *err)
 {
+    // the attention call that usually follows may be scheduled now: it waits
+    // for this grid before touching the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // strides arrive in 16-byte units
     const int64_t total = num_tokens * num_kv_heads * 2 * vecs_per_row;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;

@@ -441,6 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     constexpr int NBARS = B_VZ + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
+    // Launched with programmatic stream serialization: nothing below reads
+    // global memory before the preceding grid of the stream has completed.
+    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by indexing the shared array so the
     // compiler keeps every access in the shared state space
@@ -1275,13 +1278,17 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = pl.cl == 2 ? smem_bytes<DH, true>() : smem_bytes<DH, false>();
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)pl.cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    // the kernel may be scheduled while the preceding kernel (typically the
+    // cache write) still runs; it waits for it before its first global read
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)pl.cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pl.cl == 2 ? 1 : 0;
+    cfg.numAttrs = pl.cl == 2 ? 2 : 1;
     if (pl.cl == 2)
         return cudaLaunchKernelEx(&cfg, attn_kernel<DH, true>, p);
     return cudaLaunchKernelEx(&cfg, attn_kernel<DH, false>, p);

@@ -56,6 +56,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     constexpr int B_FIN = B_XE + 2, B_PROD = B_FIN + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
+    // launched with programmatic stream serialization: no global read before
+    // the preceding grid of the stream has completed
+    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sK = smem;
@@ -530,8 +533,17 @@ cudaError_t launch_attention512(const AttnArgs &a, const AttnPlan &pl, ErrState 
     p.max_seq_len = a.max_seq_len;
     p.split = 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    attn512_kernel<<<(unsigned)pl.grid, 512, d512::smem_bytes(), stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(512);
+    cfg.dynamicSmemBytes = d512::smem_bytes();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn512_kernel, p);
 }
 
 }  // namespace pa
