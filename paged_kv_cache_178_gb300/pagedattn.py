@@ -8,6 +8,8 @@ fails, an exception is raised.
     reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)
     paged_attention(q, k_cache, v_cache, block_tables, seq_lens,
                     query_start_loc, scale, max_query_len, max_seq_len)
+    prepare_reshape_and_cache(...) / prepare_paged_attention(...)
+        the same calls validated once, re-issued by calling the result
 
 k_cache / v_cache are [num_blocks, 16, Hkv, Dh] BF16 views (they may be
 slices of one interleaved [num_blocks, 2, 16, Hkv, Dh] pool) with identical
@@ -223,6 +225,81 @@ def paged_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), seq_lens.numel(),
         int(max_query_len), int(max_seq_len), float(scale), out.data_ptr(),
         lse.data_ptr() if lse is not None else 0, _stream_handle(stream)))
+
+
+class PreparedCall:
+    """A library call validated and marshalled once.  Calling it re-issues the
+    same C-ABI call with the same pointers: the tensors' contents may change
+    between calls, their storage must stay alive and in place (the object
+    keeps references to them)."""
+
+    def __init__(self, fn, args, what: str, keep):
+        self._fn, self._args, self._what, self._keep = fn, args, what, keep
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != PA_OK:
+            raise PagedAttnError(st, self._what)
+
+
+def prepare_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                              v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                              stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """reshape_and_cache, validated now and issued by each call of the result."""
+    c = cache_struct(k_cache, v_cache)
+    for t in (key, value):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3 or t.stride(2) != 1 \
+                or t.stride(1) != t.shape[2]:
+            raise ValueError("key/value must be [N, Hkv, Dh] BF16 CUDA tensors with contiguous heads")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 CUDA tensor")
+    n = key.shape[0]
+    if value.shape[0] != n or slot_mapping.numel() != n:
+        raise ValueError("key, value and slot_mapping disagree on the token count")
+    lib = load()
+    args = (key.data_ptr(), key.stride(0), value.data_ptr(), value.stride(0), n, ctypes.byref(c),
+            slot_mapping.data_ptr(), _stream_handle(stream))
+    return PreparedCall(lib.pa_reshape_and_cache, args, "pa_reshape_and_cache",
+                        (key, value, k_cache, v_cache, slot_mapping, c))
+
+
+def prepare_paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                            query_start_loc: torch.Tensor, scale: float, max_query_len: int,
+                            max_seq_len: int, out: torch.Tensor, lse: Optional[torch.Tensor],
+                            workspace: Optional[torch.Tensor],
+                            stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """paged_attention into given out / lse / workspace, validated now and
+    issued by each call of the result."""
+    c = cache_struct(k_cache, v_cache)
+    if q.dtype != torch.bfloat16 or not q.is_cuda or q.dim() != 3 or q.stride(2) != 1 \
+            or q.stride(1) != q.shape[2]:
+        raise ValueError("q must be a [Tq, Hq, Dh] BF16 CUDA tensor with contiguous heads")
+    tq, hq, dh = q.shape
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("query_start_loc", query_start_loc)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    num_seqs = seq_lens.numel()
+    if query_start_loc.numel() != num_seqs + 1 or block_tables.dim() != 2 \
+            or block_tables.shape[0] != num_seqs:
+        raise ValueError("metadata shapes disagree")
+    if out.shape != (tq, hq, dh) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [Tq, Hq, Dh] BF16 tensor")
+    if lse is not None and (lse.shape != (tq, hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous [Tq, Hq] fp32 tensor")
+    need = workspace_size(num_seqs, hq, c.num_kv_heads, dh, max_query_len, max_seq_len)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if ws_len < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    lib = load()
+    args = (q.data_ptr(), tq, q.stride(0), hq, ctypes.byref(c), block_tables.data_ptr(),
+            block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), num_seqs,
+            int(max_query_len), int(max_seq_len), ctypes.c_float(float(scale)), out.data_ptr(),
+            lse.data_ptr() if lse is not None else 0, workspace.data_ptr() if workspace is not None else 0,
+            ws_len, _stream_handle(stream))
+    return PreparedCall(lib.pa_paged_attention, args, "pa_paged_attention",
+                        (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, out, lse, workspace, c))
 
 
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
