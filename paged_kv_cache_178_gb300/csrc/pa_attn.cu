@@ -164,7 +164,14 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
 {
     const int tid = threadIdx.x, nth = blockDim.x;
     if (tid == 0) {
-        const uint32_t old = atomicAdd(p.ws_cnt + unit_q, 1u);
+        // acquire-release at GPU scope: releases this CTA's partial record
+        // (written before the CTA barrier that precedes this call) and, for
+        // the last arrival, acquires every other CTA's
+        uint32_t old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(p.ws_cnt + unit_q)
+                     : "memory");
         const int last = (old == (uint32_t)(nchunks - 1));
         if (last)
             p.ws_cnt[unit_q] = 0u;  // leave the workspace ready for the next call
@@ -173,7 +180,6 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
     __syncthreads();
     if (!*flag_last)
         return;
-    __threadfence();
     const int R = p.ws_rows;
     const int64_t hdr = part_header_floats(R);
     const int64_t ustride = part_record_floats(R, DH);
@@ -1080,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
                     }
                 }
-                __threadfence();
+                // ordered before the arrival's release by the CTA barrier ahead of it
             } else if (final_chunk) {
                 // epilogue: out = fold(acc, chunk) / l
                 const Fold f = fold_coef(m_acc, l_acc, m, l);
