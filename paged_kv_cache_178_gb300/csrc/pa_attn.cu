@@ -435,14 +435,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     constexpr int CHUNK_DIV = CHUNKED ? C::kChunk : 1;  // divisor used only when CHUNKED
     constexpr int TPC = CHUNKED ? C::kChunk / kKeys : 1;  // tiles per chunk
     constexpr uint32_t ACC_COL = C::kAccCol < 0 ? 0u : (uint32_t)C::kAccCol;
-    constexpr bool OBUF2 = acc_in_smem<DH, PAIR>();  // two chunk accumulators, folded one in smem
+    constexpr bool ACC_SMEM = acc_in_smem<DH, PAIR>();  // folded accumulator in shared memory
+    constexpr bool OBUF2 = ACC_SMEM;                        // two chunk accumulators (by chunk parity)
+    constexpr int NSB = 2;                                  // S/P buffers in TMEM
     // TMEM column of chunk k's accumulator
     auto ocol = [](int k) { return (uint32_t)C::kOCol + (OBUF2 ? (uint32_t)(k & 1) * 128u : 0u); };
     constexpr uint32_t ID_QK = idesc_bf16_f32(CL * kRows, kKeys, false);
     constexpr uint32_t ID_PV = idesc_bf16_f32(CL * kRows, DH, true);
     // barrier slots
     constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
-    constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_CR = B_PV + 2;
+    constexpr int B_SF = B_VE + NSV, B_PF = B_SF + NSB, B_PV = B_PF + NSB, B_CR = B_PV + 2;
     constexpr int B_OF = B_CR + 2, B_PROD = B_OF + (OBUF2 ? 2 : 1), B_DONE = B_PROD + 1, B_VZ = B_DONE + 1;
     constexpr int NBARS = B_VZ + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
@@ -560,9 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             mbar_init(bar(B_VF + s), PAIR && leader ? 2 : 1);
             mbar_init(bar(B_VE + s), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NSB; ++i) {
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_PF + i), 8 * CL);  // softmax warps of every CTA of the pair
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_PV + i), 1);
             mbar_init(bar(B_CR + i), 8);
         }
@@ -771,12 +775,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer --
-        // With two or more V stages, PV(j) and QK(j+2) are issued back to back
-        // (K(j+2) is waited for first), so the tensor pipe goes from one group
-        // to the next without idling.  QK(j+2) overwrites the S buffer that
-        // PV(j) reads P from: tcgen05 MMAs from one thread run in order.  With
-        // one V stage, K(j+2) is loaded only after PV(j) has released V, so
-        // the order is QK(j+1), PV(j).
+        // With two or more V stages, PV(j) and QK(j+NSB) are issued back to
+        // back (K(j+NSB) is waited for first), so the tensor pipe goes from one
+        // group to the next without idling and Q.K^T runs NSB tiles ahead of
+        // P.V.  QK(j+NSB) overwrites the S buffer that PV(j) reads P from:
+        // tcgen05 MMAs from one thread run in order.  With one V stage, K(j+2)
+        // is loaded only after PV(j) has released V, so the order is QK(j+1),
+        // PV(j).
         constexpr bool LOOKAHEAD = NSV >= 2;
         bool ok = true;
         if (lane == 0)
@@ -798,14 +803,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                     ad[i] = qd0 + (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
                     bd[i] = kd0 + (uint64_t)(((kk / 4) * KBLK + (kk % 4) * 32) >> 4);
                 }
-                mma8_ss<CL>(tmem + (uint32_t)(it & 1) * kKeys, ad, bd, ID_QK, g8 > 0 ? 1u : 0u);
+                mma8_ss<CL>(tmem + (uint32_t)(it % NSB) * kKeys, ad, bd, ID_QK, g8 > 0 ? 1u : 0u);
             }
             if (PAIR) {
                 mma_commit_pair_mc(bar(B_KE + sk), 0x3);
-                mma_commit_pair_mc(bar(B_SF + (it & 1)), 0x3);
+                mma_commit_pair_mc(bar(B_SF + (it % NSB)), 0x3);
             } else {
                 mma_commit(bar(B_KE + sk));
-                mma_commit(bar(B_SF + (it & 1)));
+                mma_commit(bar(B_SF + (it % NSB)));
             }
         };
         auto wait_kf = [&](int it) { return wb(B_KF + it % NSK, (it / NSK) & 1); };
@@ -817,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             // operands first: P of keys 0-63 sits in columns 0-31 of the S
             // buffer, keys 64-127 in columns 64-95 (each softmax half writes
             // its own); V advances 16 keys (2048 bytes) per instruction
-            const uint32_t pcol = tmem + (uint32_t)(j & 1) * kKeys;
+            const uint32_t pcol = tmem + (uint32_t)(j % NSB) * kKeys;
             const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), 16384, 1024);
             uint32_t ad[8];
             uint64_t bd[8];
@@ -835,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             // data only: CTA-scope waits suffice.
             bool okj = zero_tile(t) ? wbc(B_VZ, 0) : wb(B_VF + sv, (j / NSV) & 1);
             if (okj)
-                okj = wb(B_PF + (j & 1), (j >> 1) & 1);
+                okj = wb(B_PF + (j % NSB), (j / NSB) & 1);
             if (OBUF2) {
                 // the buffer was last read by the fold of chunk k - 2
                 if (okj && chunk_first && k >= 2)
@@ -862,13 +867,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         };
         if (lane == 0) {
             if (LOOKAHEAD) {
-                for (int it = 0; ok && it < min(2, n_it); ++it) {
+                for (int it = 0; ok && it < min(NSB, n_it); ++it) {
                     ok = wait_kf(it);
                     if (ok)
                         issue_qk(it);
                 }
                 for (int j = 0; ok && j < n_it; ++j)
-                    ok = issue_pv(j, j + 2 < n_it ? j + 2 : -1);
+                    ok = issue_pv(j, j + NSB < n_it ? j + NSB : -1);
             } else {
                 for (int it = 0; ok && it <= n_it; ++it) {
                     if (it < n_it) {
@@ -906,8 +911,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         bool failed = false;  // a wait gave up: leave the loop together with the other half
         for (int it = 0; it < n_it; ++it) {
             const int t = t_begin + it;
-            const int sb = it & 1;
-            bool okw = !failed && wb(B_SF + sb, (it >> 1) & 1);
+            const int sb = it % NSB;
+            bool okw = !failed && wb(B_SF + sb, (it / NSB) & 1);
             okw = __all_sync(0xffffffffu, okw);
             tc_fence_after();
             const int nallow = row_valid ? max(0, min(64, pos - t * kKeys - 64 * h + 1)) : 0;
@@ -1096,9 +1101,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t vc[32], va[32];
                     tmem_ld32(tmem + lane_off + ocol(k) + g * 32, vc);
-                    if (acc_live && !OBUF2)
+                    if (acc_live && !ACC_SMEM)
                         tmem_ld32(tmem + lane_off + ACC_COL + g * 32, va);
-                    if (acc_live && OBUF2)
+                    if (acc_live && ACC_SMEM)
                         acc_row_load<DH>(sAcc, r, g, va);
                     tmem_wait_ld();
 #pragma unroll
@@ -1121,9 +1126,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 for (int g = 0; g < DH / 32; ++g) {
                     uint32_t vc[32], va[32];
                     tmem_ld32(tmem + lane_off + ocol(k) + g * 32, vc);
-                    if (acc_live && !OBUF2)
+                    if (acc_live && !ACC_SMEM)
                         tmem_ld32(tmem + lane_off + ACC_COL + g * 32, va);
-                    if (acc_live && OBUF2)
+                    if (acc_live && ACC_SMEM)
                         acc_row_load<DH>(sAcc, r, g, va);
                     tmem_wait_ld();
 #pragma unroll
@@ -1131,12 +1136,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                         const float oa = acc_live ? __uint_as_float(va[i]) : 0.f;
                         va[i] = __float_as_uint(fold_elem(oa, __uint_as_float(vc[i]), f));
                     }
-                    if (OBUF2)
+                    if (ACC_SMEM)
                         acc_row_store<DH>(sAcc, r, g, va);
                     else
                         tmem_st32(tmem + lane_off + ACC_COL + g * 32, va);
                 }
-                if (!OBUF2)
+                if (!ACC_SMEM)
                     tmem_wait_st();
                 m_acc = f.m;
                 l_acc = f.l;
