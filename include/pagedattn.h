@@ -211,6 +211,34 @@ PA_API pa_status pa_paged_attention_noalloc(const void *q, int64_t num_q_tokens,
                                             float scale, void *out, float *lse, pa_stream_t stream);
 
 /*
+ * The whole composition of [C] What changed in one call: ReshapeAndCache of
+ * the num_new_tokens new tokens, then PagedAttention over the updated pool.
+ * The arguments and results are those of pa_reshape_and_cache followed by
+ * pa_paged_attention on `stream` (same meaning, layout and ownership); the
+ * outputs are bitwise identical to that pair of calls.
+ *   - Both argument sets are validated before anything is launched.
+ *   - What it adds: the attention grid is scheduled while the cache write
+ *     still runs.  It reads the metadata, the block tables and q and sets up
+ *     its pipeline at once; only its K/V copies wait until the cache write
+ *     has completed and its stores are visible.
+ *   - For that reason q, block_tables, seq_lens and query_start_loc must not
+ *     share bytes with the pool, and out, lse and the workspace must share
+ *     none with the pool, key, value or slot_mapping.  An overlap returns
+ *     PA_ERR_INVALID_ARG and launches nothing.
+ *   - num_new_tokens == 0 launches only the attention, which then waits for
+ *     whatever precedes it on the stream like pa_paged_attention.  An empty
+ *     attention batch launches only the cache write.
+ *   - Head dim 512 always waits at entry (no early reads).
+ */
+PA_API pa_status pa_reshape_and_paged_attention(
+    const void *key, int64_t key_tok_stride, const void *value, int64_t value_tok_stride,
+    int64_t num_new_tokens, const int64_t *slot_mapping, const void *q, int64_t num_q_tokens,
+    int64_t q_tok_stride, int32_t num_q_heads, const pa_kv_cache *cache, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+    int32_t max_query_len, int32_t max_seq_len, float scale, void *out, float *lse, void *workspace,
+    size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * flag.  Returns PA_OK, PA_ERR_BAD_METADATA or PA_ERR_TIMEOUT (or
  * PA_ERR_CUDA if the synchronisation failed).  *first_bad_index (may be

@@ -158,42 +158,167 @@ void pa_last_launch_info(char *buf, size_t n)
 
 pa_status pa_init(void) { return device_setup(nullptr); }
 
+// Cache-write arguments after validation.
+struct ReshapeCall {
+    const void *key, *value;
+    int64_t key_tok_stride, value_tok_stride, num_tokens;
+    const pa_kv_cache *cache;
+    const int64_t *slot_mapping;
+};
+
+static pa_status reshape_check(const ReshapeCall &c)
+{
+    pa_status st = check_cache(c.cache);
+    if (st != PA_OK)
+        return st;
+    if (c.num_tokens < 0)
+        return PA_ERR_INVALID_ARG;
+    if (c.num_tokens == 0)
+        return PA_OK;
+    const int64_t row = (int64_t)c.cache->num_kv_heads * c.cache->head_dim;
+    if (!c.key || !c.value || !c.slot_mapping || !aligned16(c.key) || !aligned16(c.value))
+        return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(c.slot_mapping) & 7u) != 0)
+        return PA_ERR_INVALID_ARG;
+    if (c.key_tok_stride < row || c.value_tok_stride < row || (c.key_tok_stride & 7) || (c.value_tok_stride & 7))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+static pa_status reshape_launch(const ReshapeCall &c, ErrState *err, cudaStream_t stream, char *info,
+                                size_t info_len)
+{
+    if (c.num_tokens == 0) {
+        snprintf(info, info_len, "reshape_and_cache tokens=0 (nothing launched)");
+        return PA_OK;
+    }
+    const pa_kv_cache *cache = c.cache;
+    const int vecs = cache->head_dim / 8;
+    const int64_t total = c.num_tokens * cache->num_kv_heads * 2 * vecs;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16)
+        blocks = 152 * 16;
+    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(c.key), c.key_tok_stride / 8, static_cast<const uint4 *>(c.value),
+        c.value_tok_stride / 8, c.num_tokens, cache->num_kv_heads, vecs, static_cast<uint4 *>(cache->k),
+        static_cast<uint4 *>(cache->v), cache->num_blocks * 16, cache->block_stride / 8, cache->token_stride / 8,
+        cache->head_stride / 8, c.slot_mapping, err);
+    snprintf(info, info_len, "reshape_and_cache tokens=%lld grid=%lld block=256", (long long)c.num_tokens,
+             (long long)blocks);
+    return cuda_status(cudaGetLastError());
+}
+
+// Validates an attention call and fills the kernel arguments and the plan.
+// *empty is set when there is nothing to launch.
+static pa_status attention_check(const void *q, int64_t num_q_tokens, int64_t q_tok_stride, int32_t num_q_heads,
+                                 const pa_kv_cache *cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                                 int32_t max_query_len, int32_t max_seq_len, float scale, void *out, float *lse,
+                                 void *workspace, size_t workspace_bytes, AttnArgs *a, AttnPlan *pl, bool *empty)
+{
+    *empty = false;
+    pa_status st = check_cache(cache);
+    if (st != PA_OK)
+        return st;
+    if (num_q_heads <= 0 || num_seqs < 0 || max_query_len < 0 || max_seq_len < 0 || num_q_tokens < 0 ||
+        max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % cache->num_kv_heads != 0 || num_q_heads / cache->num_kv_heads > 128)
+        return PA_ERR_UNSUPPORTED;
+    if (!(scale > 0.f) || scale == INFINITY)  // also rejects NaN
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_q_tokens == 0 || max_query_len == 0) {
+        *empty = true;
+        return PA_OK;
+    }
+    const int64_t row = (int64_t)num_q_heads * cache->head_dim;
+    if (!q || !out || !block_tables || !seq_lens || !query_start_loc || !aligned16(q) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return PA_ERR_INVALID_ARG;
+    if (q_tok_stride < row || (q_tok_stride & 7) || num_q_tokens > ((int64_t)1 << 31) - 1)
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq == 0)
+        return PA_ERR_INVALID_ARG;
+    if (!plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
+                        pl))
+        return PA_ERR_UNSUPPORTED;
+    if (pl->ws_bytes > 0) {
+        if (!workspace || workspace_bytes < pl->ws_bytes)
+            return PA_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return PA_ERR_INVALID_ARG;
+    }
+    a->q = q;
+    a->num_q_tokens = num_q_tokens;
+    a->q_tok_stride = q_tok_stride;
+    a->num_q_heads = num_q_heads;
+    a->k = cache->k;
+    a->v = cache->v;
+    a->num_blocks = cache->num_blocks;
+    a->num_kv_heads = cache->num_kv_heads;
+    a->head_dim = cache->head_dim;
+    a->block_stride = cache->block_stride;
+    a->token_stride = cache->token_stride;
+    a->head_stride = cache->head_stride;
+    a->block_tables = block_tables;
+    a->max_blocks_per_seq = max_blocks_per_seq;
+    a->seq_lens = seq_lens;
+    a->query_start_loc = query_start_loc;
+    a->num_seqs = num_seqs;
+    a->max_query_len = max_query_len;
+    a->max_seq_len = max_seq_len;
+    a->scale = scale;
+    a->out = out;
+    a->lse = lse;
+    a->workspace = workspace;
+    a->workspace_bytes = workspace_bytes;
+    a->early_reads = false;
+    return PA_OK;
+}
+
+static pa_status attention_launch(const AttnArgs &a, const AttnPlan &pl, ErrState *err, cudaStream_t stream,
+                                  char *info, size_t info_len)
+{
+    cudaError_t e = launch_attention(a, pl, err, stream, info, info_len);
+    if (e == cudaErrorNotSupported)
+        return PA_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+// Half-open byte range [lo, hi) of a device buffer.
+struct Span {
+    uintptr_t lo, hi;
+};
+
+static Span span(const void *p, int64_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Span{lo, lo + (uintptr_t)(bytes > 0 ? bytes : 0)};
+}
+
+static bool overlaps(const Span &x, const Span &y) { return x.lo < y.hi && y.lo < x.hi; }
+
+// Bytes spanned by one view of the pool (K or V).
+static int64_t pool_view_bytes(const pa_kv_cache *c)
+{
+    return ((c->num_blocks - 1) * c->block_stride + 15 * c->token_stride +
+            (int64_t)(c->num_kv_heads - 1) * c->head_stride + c->head_dim) *
+           2;
+}
+
 pa_status pa_reshape_and_cache(const void *key, int64_t key_tok_stride, const void *value,
                                int64_t value_tok_stride, int64_t num_tokens, const pa_kv_cache *cache,
                                const int64_t *slot_mapping, pa_stream_t stream)
 {
-    pa_status st = check_cache(cache);
+    const ReshapeCall c{key, value, key_tok_stride, value_tok_stride, num_tokens, cache, slot_mapping};
+    pa_status st = reshape_check(c);
     if (st != PA_OK)
         return st;
-    if (num_tokens < 0)
-        return PA_ERR_INVALID_ARG;
-    if (num_tokens == 0) {
-        snprintf(g_last_info, sizeof g_last_info, "reshape_and_cache tokens=0 (nothing launched)");
-        return PA_OK;
-    }
-    const int64_t row = (int64_t)cache->num_kv_heads * cache->head_dim;
-    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
-        return PA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
-        return PA_ERR_INVALID_ARG;
-    if (key_tok_stride < row || value_tok_stride < row || (key_tok_stride & 7) || (value_tok_stride & 7))
-        return PA_ERR_INVALID_ARG;
     ErrState *err = nullptr;
-    if ((st = device_setup(&err)) != PA_OK)
+    if (num_tokens > 0 && (st = device_setup(&err)) != PA_OK)
         return st;
-    const int vecs = cache->head_dim / 8;
-    const int64_t total = num_tokens * cache->num_kv_heads * 2 * vecs;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16)
-        blocks = 152 * 16;
-    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(key), key_tok_stride / 8, static_cast<const uint4 *>(value),
-        value_tok_stride / 8, num_tokens, cache->num_kv_heads, vecs, static_cast<uint4 *>(cache->k),
-        static_cast<uint4 *>(cache->v), cache->num_blocks * 16, cache->block_stride / 8,
-        cache->token_stride / 8, cache->head_stride / 8, slot_mapping, err);
-    snprintf(g_last_info, sizeof g_last_info, "reshape_and_cache tokens=%lld grid=%lld block=256",
-             (long long)num_tokens, (long long)blocks);
-    return cuda_status(cudaGetLastError());
+    return reshape_launch(c, err, reinterpret_cast<cudaStream_t>(stream), g_last_info, sizeof g_last_info);
 }
 
 size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -211,72 +336,94 @@ pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_
                              int32_t max_query_len, int32_t max_seq_len, float scale, void *out, float *lse,
                              void *workspace, size_t workspace_bytes, pa_stream_t stream)
 {
-    pa_status st = check_cache(cache);
+    AttnArgs a;
+    AttnPlan pl;
+    bool empty = false;
+    pa_status st = attention_check(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables,
+                                   max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, max_query_len,
+                                   max_seq_len, scale, out, lse, workspace, workspace_bytes, &a, &pl, &empty);
     if (st != PA_OK)
         return st;
-    if (num_q_heads <= 0 || num_seqs < 0 || max_query_len < 0 || max_seq_len < 0 || num_q_tokens < 0 ||
-        max_blocks_per_seq < 0)
-        return PA_ERR_INVALID_ARG;
-    if (num_q_heads % cache->num_kv_heads != 0 || num_q_heads / cache->num_kv_heads > 128)
-        return PA_ERR_UNSUPPORTED;
-    if (!(scale > 0.f) || scale == INFINITY)  // also rejects NaN
-        return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0 || num_q_tokens == 0 || max_query_len == 0) {
+    if (empty) {
         snprintf(g_last_info, sizeof g_last_info, "attention: empty batch (nothing launched)");
         return PA_OK;
-    }
-    const int64_t row = (int64_t)num_q_heads * cache->head_dim;
-    if (!q || !out || !block_tables || !seq_lens || !query_start_loc || !aligned16(q) || !aligned16(out))
-        return PA_ERR_INVALID_ARG;
-    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return PA_ERR_INVALID_ARG;
-    if (q_tok_stride < row || (q_tok_stride & 7) || num_q_tokens > ((int64_t)1 << 31) - 1)
-        return PA_ERR_INVALID_ARG;
-    if (max_blocks_per_seq == 0)
-        return PA_ERR_INVALID_ARG;
-    AttnPlan pl;
-    if (!plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
-                        &pl))
-        return PA_ERR_UNSUPPORTED;
-    if (pl.ws_bytes > 0) {
-        if (!workspace || workspace_bytes < pl.ws_bytes)
-            return PA_ERR_WORKSPACE;
-        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-            return PA_ERR_INVALID_ARG;
     }
     ErrState *err = nullptr;
     if ((st = device_setup(&err)) != PA_OK)
         return st;
+    return attention_launch(a, pl, err, reinterpret_cast<cudaStream_t>(stream), g_last_info, sizeof g_last_info);
+}
+
+pa_status pa_reshape_and_paged_attention(const void *key, int64_t key_tok_stride, const void *value,
+                                         int64_t value_tok_stride, int64_t num_new_tokens,
+                                         const int64_t *slot_mapping, const void *q, int64_t num_q_tokens,
+                                         int64_t q_tok_stride, int32_t num_q_heads, const pa_kv_cache *cache,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *seq_lens, const int32_t *query_start_loc,
+                                         int32_t num_seqs, int32_t max_query_len, int32_t max_seq_len,
+                                         float scale, void *out, float *lse, void *workspace,
+                                         size_t workspace_bytes, pa_stream_t stream)
+{
+    // Validate both calls before launching either.
+    const ReshapeCall c{key, value, key_tok_stride, value_tok_stride, num_new_tokens, cache, slot_mapping};
+    pa_status st = reshape_check(c);
+    if (st != PA_OK)
+        return st;
     AttnArgs a;
-    a.q = q;
-    a.num_q_tokens = num_q_tokens;
-    a.q_tok_stride = q_tok_stride;
-    a.num_q_heads = num_q_heads;
-    a.k = cache->k;
-    a.v = cache->v;
-    a.num_blocks = cache->num_blocks;
-    a.num_kv_heads = cache->num_kv_heads;
-    a.head_dim = cache->head_dim;
-    a.block_stride = cache->block_stride;
-    a.token_stride = cache->token_stride;
-    a.head_stride = cache->head_stride;
-    a.block_tables = block_tables;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.seq_lens = seq_lens;
-    a.query_start_loc = query_start_loc;
-    a.num_seqs = num_seqs;
-    a.max_query_len = max_query_len;
-    a.max_seq_len = max_seq_len;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    a.workspace = workspace;
-    a.workspace_bytes = workspace_bytes;
-    cudaError_t e = launch_attention(a, pl, err, reinterpret_cast<cudaStream_t>(stream), g_last_info,
-                                     sizeof g_last_info);
-    if (e == cudaErrorNotSupported)
-        return PA_ERR_UNSUPPORTED;
-    return cuda_status(e);
+    AttnPlan pl;
+    bool empty = false;
+    st = attention_check(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables, max_blocks_per_seq,
+                         seq_lens, query_start_loc, num_seqs, max_query_len, max_seq_len, scale, out, lse,
+                         workspace, workspace_bytes, &a, &pl, &empty);
+    if (st != PA_OK)
+        return st;
+    if (!empty && num_new_tokens > 0) {
+        // The attention grid reads q and the metadata, and writes out, lse
+        // and the workspace, while the cache write may still run: none of
+        // them may share bytes with what the cache write reads or writes.
+        const int64_t kv_row = (int64_t)cache->num_kv_heads * cache->head_dim;
+        const Span writes_of_write[2] = {span(cache->k, pool_view_bytes(cache)),
+                                         span(cache->v, pool_view_bytes(cache))};
+        const Span reads_of_write[3] = {span(key, ((num_new_tokens - 1) * key_tok_stride + kv_row) * 2),
+                                        span(value, ((num_new_tokens - 1) * value_tok_stride + kv_row) * 2),
+                                        span(slot_mapping, num_new_tokens * 8)};
+        const Span early_reads[4] = {
+            span(q, ((num_q_tokens - 1) * q_tok_stride + (int64_t)num_q_heads * cache->head_dim) * 2),
+            span(block_tables, (int64_t)num_seqs * max_blocks_per_seq * 4), span(seq_lens, (int64_t)num_seqs * 4),
+            span(query_start_loc, ((int64_t)num_seqs + 1) * 4)};
+        const Span attn_writes[3] = {span(out, num_q_tokens * num_q_heads * (int64_t)cache->head_dim * 2),
+                                     span(lse, lse ? num_q_tokens * num_q_heads * 4 : 0),
+                                     span(workspace, (int64_t)pl.ws_bytes)};
+        for (const Span &w : writes_of_write)
+            for (const Span &r : early_reads)
+                if (overlaps(w, r))
+                    return PA_ERR_INVALID_ARG;
+        for (const Span &w : attn_writes) {
+            for (const Span &x : writes_of_write)
+                if (overlaps(w, x))
+                    return PA_ERR_INVALID_ARG;
+            for (const Span &x : reads_of_write)
+                if (overlaps(w, x))
+                    return PA_ERR_INVALID_ARG;
+        }
+    }
+    ErrState *err = nullptr;
+    if ((st = device_setup(&err)) != PA_OK)
+        return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char info_w[128], info_a[192];
+    if ((st = reshape_launch(c, err, s, info_w, sizeof info_w)) != PA_OK)
+        return st;
+    if (empty) {
+        snprintf(g_last_info, sizeof g_last_info, "%.80s; attention: empty batch (nothing launched)", info_w);
+        return PA_OK;
+    }
+    // Only a cache write launched just before makes the early reads safe;
+    // the head-dim 512 kernel always waits at entry.
+    a.early_reads = num_new_tokens > 0 && cache->head_dim != 512;
+    st = attention_launch(a, pl, err, s, info_a, sizeof info_a);
+    snprintf(g_last_info, sizeof g_last_info, "%.80s; %.160s%s", info_w, info_a, a.early_reads ? " early_reads" : "");
+    return st;
 }
 
 // Scratch for pa_paged_attention_noalloc: lives in the library image, so

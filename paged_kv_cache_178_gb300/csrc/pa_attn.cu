@@ -449,9 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     constexpr int NBARS = B_VZ + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
-    // Launched with programmatic stream serialization: nothing below reads
-    // global memory before the preceding grid of the stream has completed.
-    griddep_wait();
+    // Launched with programmatic stream serialization.  By default nothing
+    // below reads global memory before the preceding grid of the stream has
+    // completed.  With early_reads the preceding grid writes only the K/V
+    // pool: metadata, block tables and Q are read at once and the producer
+    // waits just before its first K/V copy.
+    if (!p.early_reads)
+        griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by indexing the shared array so the
     // compiler keeps every access in the shared state space
@@ -624,6 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 tma_load_3d(smem_addr(sQ + lane * 16384), &p.tm_q, bar(B_Q), lane * 64, kvh * p.group,
                             (int)tok_first);
         }
+        if (p.early_reads)
+            griddep_wait();  // the cache write has completed and is visible
         // ids of tiles (2j, 2j+1) sit in lanes 0-15 of ids_cur; the next pair is
         // requested one pair ahead
         int ids_next = 0;
@@ -1282,6 +1288,7 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.ws_rows = pl.ws_rows;
     p.split = pl.split ? 1 : 0;
     p.npairs = (pl.qtiles + 1) / 2;
+    p.early_reads = a.early_reads ? 1 : 0;
     // C2: scale * log2(e) formed once, in fp32, on the host
     p.scale_log2 = a.scale * 1.4426950408889634f;
     cudaLaunchConfig_t cfg = {};

@@ -37,6 +37,7 @@ struct AttnParams {
     int32_t ws_rows;
     int32_t split;
     int32_t npairs;  // query-tile pairs (in-CTA schedule on CTA pairs)
+    int32_t early_reads;  // only the K/V copies wait for the preceding grid
     float scale_log2;
 };
 

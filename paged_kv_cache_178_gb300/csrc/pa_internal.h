@@ -48,6 +48,9 @@ struct AttnArgs {
     float *lse;
     void *workspace;
     size_t workspace_bytes;
+    // The preceding kernel of the stream writes only the K/V pool: the
+    // kernel may read everything else before that kernel has finished.
+    bool early_reads;
 };
 
 // Work decomposition chosen from host scalars only.

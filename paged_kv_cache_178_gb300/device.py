@@ -71,6 +71,16 @@ class DeviceWorkload:
             self.query_start_loc if query_start_loc is None else query_start_loc,
             self.w.scale, mq, ms, out=out, lse=lse, want_lse=want_lse, workspace=ws, stream=stream)
 
+    def write_and_attend(self, key=None, value=None, slot_mapping=None, out=None, lse=None, want_lse=True,
+                         stream=None):
+        """The cache write of (key, value, slot_mapping) -- by default every
+        token of the workload -- and the attention, in one library call."""
+        return pagedattn.reshape_and_paged_attention(
+            self.key if key is None else key, self.value if value is None else value,
+            self.slot_mapping if slot_mapping is None else slot_mapping, self.q, self.k_cache, self.v_cache,
+            self.block_tables, self.seq_lens, self.query_start_loc, self.w.scale, self.max_query_len,
+            self.max_seq_len, out=out, lse=lse, want_lse=want_lse, workspace=self.workspace, stream=stream)
+
     def share_cache_with(self, other: "DeviceWorkload") -> None:
         """Point this workload at another's pool (same geometry)."""
         self.pool, self.k_cache, self.v_cache = other.pool, other.k_cache, other.v_cache

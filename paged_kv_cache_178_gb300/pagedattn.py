@@ -36,7 +36,8 @@ PA_ERR_TIMEOUT = 5
 PA_ERR_CUDA = 6
 
 EXPORTED = ("pa_init", "pa_reshape_and_cache", "pa_paged_attention_workspace_size",
-            "pa_paged_attention", "pa_paged_attention_noalloc", "pa_check_errors",
+            "pa_paged_attention", "pa_paged_attention_noalloc", "pa_reshape_and_paged_attention",
+            "pa_check_errors",
             "pa_status_string", "pa_last_launch_info")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -82,6 +83,10 @@ def load(path: str = LIB_PATH):
         lib.pa_paged_attention_noalloc.restype = i32
         lib.pa_paged_attention_noalloc.argtypes = [vp, i64, i64, i32, ctypes.POINTER(PaKvCache), vp, i32,
                                                    vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
+        lib.pa_reshape_and_paged_attention.restype = i32
+        lib.pa_reshape_and_paged_attention.argtypes = [
+            vp, i64, vp, i64, i64, vp, vp, i64, i64, i32, ctypes.POINTER(PaKvCache), vp, i32, vp, vp, i32,
+            i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
         lib.pa_check_errors.restype = i32
         lib.pa_check_errors.argtypes = [vp, ctypes.POINTER(i64)]
         lib.pa_status_string.restype = ctypes.c_char_p
@@ -130,12 +135,8 @@ def cache_struct(k_cache: torch.Tensor, v_cache: torch.Tensor) -> PaKvCache:
                      k_cache.stride(1), k_cache.stride(2))
 
 
-def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
-                      v_cache: torch.Tensor, slot_mapping: torch.Tensor,
-                      stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Write key/value [N, Hkv, Dh] into the caches at slot_mapping [N] (int64);
-    negative slots are skipped."""
-    c = cache_struct(k_cache, v_cache)
+def _validate_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor) -> int:
+    """Checks the cache-write inputs; returns the token count."""
     for t in (key, value):
         if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3 or t.stride(2) != 1 \
                 or t.stride(1) != t.shape[2]:
@@ -145,6 +146,34 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
     n = key.shape[0]
     if value.shape[0] != n or slot_mapping.numel() != n:
         raise ValueError("key, value and slot_mapping disagree on the token count")
+    return n
+
+
+def _validate_attention(q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                        query_start_loc: torch.Tensor) -> Tuple[int, int, int, int]:
+    """Checks the attention inputs; returns (Tq, Hq, Dh, num_seqs)."""
+    if q.dtype != torch.bfloat16 or not q.is_cuda or q.dim() != 3 or q.stride(2) != 1 \
+            or q.stride(1) != q.shape[2]:
+        raise ValueError("q must be a [Tq, Hq, Dh] BF16 CUDA tensor with contiguous heads")
+    tq, hq, dh = q.shape
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("query_start_loc", query_start_loc)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    num_seqs = seq_lens.numel()
+    if query_start_loc.numel() != num_seqs + 1 or block_tables.dim() != 2 \
+            or block_tables.shape[0] != num_seqs:
+        raise ValueError("metadata shapes disagree")
+    return tq, hq, dh, num_seqs
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write key/value [N, Hkv, Dh] into the caches at slot_mapping [N] (int64);
+    negative slots are skipped."""
+    c = cache_struct(k_cache, v_cache)
+    n = _validate_write(key, value, slot_mapping)
     _check(load().pa_reshape_and_cache(key.data_ptr(), key.stride(0), value.data_ptr(), value.stride(0),
                                        n, ctypes.byref(c), slot_mapping.data_ptr(),
                                        _stream_handle(stream)), "pa_reshape_and_cache")
@@ -174,18 +203,7 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     """Causal GQA attention of q [Tq, Hq, Dh] over the paged caches.
     Returns (out [Tq, Hq, Dh] BF16, lse [Tq, Hq] fp32 or None)."""
     c = cache_struct(k_cache, v_cache)
-    if q.dtype != torch.bfloat16 or not q.is_cuda or q.dim() != 3 or q.stride(2) != 1 \
-            or q.stride(1) != q.shape[2]:
-        raise ValueError("q must be a [Tq, Hq, Dh] BF16 CUDA tensor with contiguous heads")
-    tq, hq, dh = q.shape
-    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
-                    ("query_start_loc", query_start_loc)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
-    num_seqs = seq_lens.numel()
-    if query_start_loc.numel() != num_seqs + 1 or block_tables.dim() != 2 \
-            or block_tables.shape[0] != num_seqs:
-        raise ValueError("metadata shapes disagree")
+    tq, hq, dh, num_seqs = _validate_attention(q, block_tables, seq_lens, query_start_loc)
     if out is None:
         out = torch.empty((tq, hq, dh), dtype=torch.bfloat16, device=q.device)
     elif out.shape != (tq, hq, dh) or out.dtype != torch.bfloat16 or not out.is_contiguous():
@@ -247,15 +265,7 @@ def prepare_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: t
                               stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
     """reshape_and_cache, validated now and issued by each call of the result."""
     c = cache_struct(k_cache, v_cache)
-    for t in (key, value):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3 or t.stride(2) != 1 \
-                or t.stride(1) != t.shape[2]:
-            raise ValueError("key/value must be [N, Hkv, Dh] BF16 CUDA tensors with contiguous heads")
-    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
-        raise ValueError("slot_mapping must be a contiguous int64 CUDA tensor")
-    n = key.shape[0]
-    if value.shape[0] != n or slot_mapping.numel() != n:
-        raise ValueError("key, value and slot_mapping disagree on the token count")
+    n = _validate_write(key, value, slot_mapping)
     lib = load()
     args = (key.data_ptr(), key.stride(0), value.data_ptr(), value.stride(0), n, ctypes.byref(c),
             slot_mapping.data_ptr(), _stream_handle(stream))
@@ -272,18 +282,7 @@ def prepare_paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     """paged_attention into given out / lse / workspace, validated now and
     issued by each call of the result."""
     c = cache_struct(k_cache, v_cache)
-    if q.dtype != torch.bfloat16 or not q.is_cuda or q.dim() != 3 or q.stride(2) != 1 \
-            or q.stride(1) != q.shape[2]:
-        raise ValueError("q must be a [Tq, Hq, Dh] BF16 CUDA tensor with contiguous heads")
-    tq, hq, dh = q.shape
-    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
-                    ("query_start_loc", query_start_loc)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
-    num_seqs = seq_lens.numel()
-    if query_start_loc.numel() != num_seqs + 1 or block_tables.dim() != 2 \
-            or block_tables.shape[0] != num_seqs:
-        raise ValueError("metadata shapes disagree")
+    tq, hq, dh, num_seqs = _validate_attention(q, block_tables, seq_lens, query_start_loc)
     if out.shape != (tq, hq, dh) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [Tq, Hq, Dh] BF16 tensor")
     if lse is not None and (lse.shape != (tq, hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
@@ -300,6 +299,73 @@ def prepare_paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
             ws_len, _stream_handle(stream))
     return PreparedCall(lib.pa_paged_attention, args, "pa_paged_attention",
                         (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, out, lse, workspace, c))
+
+
+def _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens,
+                      query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace, stream):
+    c = cache_struct(k_cache, v_cache)
+    n = _validate_write(key, value, slot_mapping)
+    tq, hq, dh, num_seqs = _validate_attention(q, block_tables, seq_lens, query_start_loc)
+    if out.shape != (tq, hq, dh) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [Tq, Hq, Dh] BF16 tensor")
+    if lse is not None and (lse.shape != (tq, hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous [Tq, Hq] fp32 tensor")
+    need = workspace_size(num_seqs, hq, c.num_kv_heads, dh, max_query_len, max_seq_len)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if ws_len < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    args = (key.data_ptr(), key.stride(0), value.data_ptr(), value.stride(0), n, slot_mapping.data_ptr(),
+            q.data_ptr(), tq, q.stride(0), hq, ctypes.byref(c), block_tables.data_ptr(),
+            block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), num_seqs,
+            int(max_query_len), int(max_seq_len), ctypes.c_float(float(scale)), out.data_ptr(),
+            lse.data_ptr() if lse is not None else 0, workspace.data_ptr() if workspace is not None else 0,
+            ws_len, _stream_handle(stream))
+    keep = (key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, out, lse,
+            workspace, c)
+    return args, keep
+
+
+def reshape_and_paged_attention(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+                                q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                query_start_loc: torch.Tensor, scale: float, max_query_len: int,
+                                max_seq_len: int, out: Optional[torch.Tensor] = None,
+                                lse: Optional[torch.Tensor] = None, want_lse: bool = True,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream: Optional[torch.cuda.Stream] = None
+                                ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """reshape_and_cache of key/value at slot_mapping, then paged_attention of q
+    over the updated caches, in one library call whose attention grid starts
+    its set-up while the cache write runs.  Returns (out, lse or None)."""
+    tq, hq, dh = q.shape
+    if out is None:
+        out = torch.empty((tq, hq, dh), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((tq, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = workspace_size(seq_lens.numel(), hq, k_cache.shape[2], dh, max_query_len, max_seq_len)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    args, _keep = _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens,
+                                    query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace,
+                                    stream)
+    _check(load().pa_reshape_and_paged_attention(*args), "pa_reshape_and_paged_attention")
+    return out, lse
+
+
+def prepare_reshape_and_paged_attention(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+                                        q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                        block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                        query_start_loc: torch.Tensor, scale: float, max_query_len: int,
+                                        max_seq_len: int, out: torch.Tensor, lse: Optional[torch.Tensor],
+                                        workspace: Optional[torch.Tensor],
+                                        stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """reshape_and_paged_attention into given out / lse / workspace, validated
+    now and issued by each call of the result."""
+    args, keep = _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens,
+                                   query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace,
+                                   stream)
+    return PreparedCall(load().pa_reshape_and_paged_attention, args, "pa_reshape_and_paged_attention", keep)
 
 
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:

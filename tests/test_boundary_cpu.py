@@ -98,6 +98,48 @@ def test_attention_validation(lib):
     assert _attn(lib, c, mq=-1) == pagedattn.PA_ERR_INVALID_ARG
 
 
+# Buffers for the one-call composition, 16 MB apart and clear of the fake
+# pool (2048 blocks x 8192 elements x 2 bytes from FAKE).
+_BUF = {name: 0x20000000 + i * 0x1000000
+        for i, name in enumerate(("key", "value", "slots", "q", "bt", "sl", "qsl", "out", "lse", "ws"))}
+
+
+def _rpa(lib, cache, **kw):
+    a = dict(_BUF)
+    a.update(kw)
+    ws_len = pagedattn.workspace_size(4, 8, 2, 128, 1, 7168)
+    return lib.pa_reshape_and_paged_attention(
+        a["key"], 256, a["value"], 256, a.get("n", 4), a["slots"], a["q"], 4, 1024, a.get("hq", 8),
+        ctypes.byref(cache), a["bt"], 448, a["sl"], a["qsl"], 4, 1, 7168, ctypes.c_float(0.088), a["out"],
+        a["lse"], a["ws"], ws_len, None)
+
+
+def test_composition_validation_and_overlap(lib):
+    import torch
+    c = _cache()
+    # either half's checks apply before anything is launched
+    assert _rpa(lib, c, key=_BUF["key"] + 8) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rpa(lib, c, hq=7) == pagedattn.PA_ERR_UNSUPPORTED
+    assert _rpa(lib, _cache(block_size=8)) == pagedattn.PA_ERR_UNSUPPORTED
+    # the attention writes out / lse / workspace while the cache write may run
+    assert _rpa(lib, c, out=FAKE + 4096) == pagedattn.PA_ERR_INVALID_ARG      # inside the pool
+    assert _rpa(lib, c, out=_BUF["key"]) == pagedattn.PA_ERR_INVALID_ARG      # over key
+    assert _rpa(lib, c, lse=_BUF["slots"] + 16) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rpa(lib, c, ws=_BUF["value"]) == pagedattn.PA_ERR_INVALID_ARG
+    # q and the metadata are read early: none may lie in the pool
+    assert _rpa(lib, c, q=FAKE + (1 << 20)) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rpa(lib, c, bt=FAKE + 256) == pagedattn.PA_ERR_INVALID_ARG
+    assert _rpa(lib, c, qsl=FAKE + 2047 * 8192 * 2) == pagedattn.PA_ERR_INVALID_ARG  # last block
+    # just past the V view's last byte is fine; sharing bytes among the
+    # read-only inputs (q over key) is fine too
+    end = FAKE + 0x1000 + (2047 * 8192 + 15 * 256 + 128 + 128) * 2
+    assert _rpa(lib, c, sl=end - 4) == pagedattn.PA_ERR_INVALID_ARG
+    ok = pagedattn.PA_OK if torch.cuda.is_available() else pagedattn.PA_ERR_CUDA
+    if not torch.cuda.is_available():
+        assert _rpa(lib, c, sl=end) == ok
+        assert _rpa(lib, c, q=_BUF["key"]) == ok
+
+
 def test_workspace_size_is_host_arithmetic(lib):
     # decode: 4 requests x 2 KV heads, one 4-row query tile each, 28 chunks
     # of 256 keys, records of (m, l, O[128]) per row + 256 B of counters
