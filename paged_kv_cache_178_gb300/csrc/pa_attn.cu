@@ -782,8 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer --
         // With two or more V stages, PV(j) and QK(j+NSB) are issued back to
-        // back (K(j+NSB) is waited for first), so the tensor pipe goes from one
-        // group to the next without idling and Q.K^T runs NSB tiles ahead of
+        // back (PV(j) first, then the wait for K(j+NSB)), so the tensor pipe
+        // goes from one group to the next and Q.K^T runs NSB tiles ahead of
         // P.V.  QK(j+NSB) overwrites the S buffer that PV(j) reads P from:
         // tcgen05 MMAs from one thread run in order.  With one V stage, K(j+2)
         // is loaded only after PV(j) has released V, so the order is QK(j+1),
@@ -854,8 +854,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             } else if (okj && chunk_first && k > 0) {
                 okj = wb(B_OF, (k - 1) & 1);
             }
-            if (okj && qk_next >= 0)
-                okj = wait_kf(qk_next);
             if (okj) {
                 tc_fence_after();
                 mma8_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
@@ -866,8 +864,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                     mma_commit(bar(B_VE + sv));
                     mma_commit(bar(B_PV + (j & 1)));
                 }
-                if (qk_next >= 0)
-                    issue_qk(qk_next);
+                // K(qk_next) may still be in flight: PV(j) does not wait for it
+                if (qk_next >= 0) {
+                    okj = wait_kf(qk_next);
+                    if (okj)
+                        issue_qk(qk_next);
+                }
             }
             return okj;
         };
@@ -933,9 +935,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 tmem_ld32(scol + 32, v1);
                 tmem_wait_ld();
                 if (unmasked) {
+                    // two independent chains of three-input max (max is exact:
+                    // the grouping does not change the result)
+                    float pm0 = -INFINITY, pm1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pmax = fmaxf(pmax, fmaxf(__uint_as_float(v0[i]), __uint_as_float(v1[i])));
+                    for (int i = 0; i < 32; i += 2) {
+                        pm0 = max3f(pm0, __uint_as_float(v0[i]), __uint_as_float(v1[i]));
+                        pm1 = max3f(pm1, __uint_as_float(v0[i + 1]), __uint_as_float(v1[i + 1]));
+                    }
+                    pmax = fmaxf(pm0, pm1);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -966,9 +974,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             // sum, P as BF16
             float hs = 0.f;
             if (warp_active) {
-                const float negm = -m_new;
-                const float c2 = p.scale_log2;
-                float a[8];
+                // columns c and c+1 go through the paired fp32 instructions:
+                // each lane is the scalar fma.rn / add.rn of the same operands
+                const uint64_t c2x2 = pack_f32x2(p.scale_log2, p.scale_log2);
+                const uint64_t nmx2 = pack_f32x2(-m_new, -m_new);
+                uint64_t a2[4];  // accumulator k sums columns k, k+8, ..., k+56 (pairs k, k+1)
                 uint32_t w[32];
 #pragma unroll
                 for (int g2 = 0; g2 < 2; ++g2) {
@@ -978,22 +988,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         const int c = g2 * 32 + i;
-                        float e0 = ex2(__fmaf_rn(__uint_as_float(v[i]), c2, negm));
-                        float e1 = ex2(__fmaf_rn(__uint_as_float(v[i + 1]), c2, negm));
+                        float x0, x1;
+                        unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                               c2x2, nmx2),
+                                     x0, x1);
+                        float e0 = ex2(x0);
+                        float e1 = ex2(x1);
                         if (!unmasked) {
                             e0 = (c < nallow) ? e0 : 0.f;
                             e1 = (c + 1 < nallow) ? e1 : 0.f;
                         }
-                        if (c < 8) {
-                            a[c & 7] = e0;
-                            a[(c + 1) & 7] = e1;
-                        } else {
-                            a[c & 7] = __fadd_rn(a[c & 7], e0);
-                            a[(c + 1) & 7] = __fadd_rn(a[(c + 1) & 7], e1);
-                        }
+                        const uint64_t e2 = pack_f32x2(e0, e1);
+                        a2[(c & 7) / 2] = (c < 8) ? e2 : add_f32x2(a2[(c & 7) / 2], e2);
                         w[c / 2] = pack_bf16x2(e0, e1);
                     }
                 }
+                float a[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2)
+                    unpack_f32x2(a2[k2], a[2 * k2], a[2 * k2 + 1]);
                 hs = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
                                __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
                 // P (BF16, two keys per column) overwrites this half's first 32 S

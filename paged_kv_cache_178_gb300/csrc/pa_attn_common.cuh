@@ -48,6 +48,44 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// Paired fp32 arithmetic (two lanes per instruction, each lane rounded
+// exactly as the scalar .rn instruction) and three-input max: the softmax's
+// instruction count, not the exp2 unit, bounds its throughput.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// {a0*b0 + c0, a1*b1 + c1}, each a single-rounding fma.rn
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// {a0 + b0, a1 + b1}, each add.rn
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Fold of two softmax states (m, l, O) -- C5.  A state with m = -inf holds
 // no key: folding it in leaves the other side unchanged, and folding into it
 // takes the other side verbatim.
