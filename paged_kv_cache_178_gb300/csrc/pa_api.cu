@@ -77,8 +77,13 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots, int64_t block_stride,
     int64_t token_stride, int64_t head_stride, const int64_t *__restrict__ slot_mapping, ErrState *err)
 {
-    // the attention call that usually follows may be scheduled now: it waits
-    // for this grid before touching the cache
+    // Launched with programmatic stream serialization: wait for the preceding
+    // grid of the stream (it may have produced key, value or slot_mapping),
+    // then let the dependent grid be scheduled.  The attention that usually
+    // follows may read its metadata and q from here on -- the grids before
+    // this one have completed -- and waits for this grid before touching the
+    // cache.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // strides arrive in 16-byte units
     const int64_t total = num_tokens * num_kv_heads * 2 * vecs_per_row;
@@ -90,6 +95,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
         rest /= 2;
         const int h = (int)(rest % num_kv_heads);
         const int64_t i = rest / num_kv_heads;
+        // the source vector does not depend on the slot: both loads are in
+        // flight together (token i's row exists whatever its slot says)
+        const uint4 src = which == 0 ? __ldg(key + i * key_tok_stride + (int64_t)h * vecs_per_row + vec)
+                                     : __ldg(value + i * value_tok_stride + (int64_t)h * vecs_per_row + vec);
         const int64_t slot = __ldg(slot_mapping + i);
         if (slot < 0)
             continue;
@@ -99,10 +108,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
             continue;
         }
         const int64_t dst = (slot >> 4) * block_stride + (slot & 15) * token_stride + h * head_stride + vec;
-        if (which == 0)
-            k_cache[dst] = __ldg(key + i * key_tok_stride + (int64_t)h * vecs_per_row + vec);
-        else
-            v_cache[dst] = __ldg(value + i * value_tok_stride + (int64_t)h * vecs_per_row + vec);
+        (which == 0 ? k_cache : v_cache)[dst] = src;
     }
 }
 
@@ -198,14 +204,24 @@ static pa_status reshape_launch(const ReshapeCall &c, ErrState *err, cudaStream_
     int64_t blocks = (total + 255) / 256;
     if (blocks > 152 * 16)
         blocks = 152 * 16;
-    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint4 *>(c.key), c.key_tok_stride / 8, static_cast<const uint4 *>(c.value),
-        c.value_tok_stride / 8, c.num_tokens, cache->num_kv_heads, vecs, static_cast<uint4 *>(cache->k),
-        static_cast<uint4 *>(cache->v), cache->num_blocks * 16, cache->block_stride / 8, cache->token_stride / 8,
-        cache->head_stride / 8, c.slot_mapping, err);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, reshape_and_cache_kernel, static_cast<const uint4 *>(c.key), (int64_t)(c.key_tok_stride / 8),
+        static_cast<const uint4 *>(c.value), (int64_t)(c.value_tok_stride / 8), c.num_tokens,
+        (int32_t)cache->num_kv_heads, (int32_t)vecs, static_cast<uint4 *>(cache->k), static_cast<uint4 *>(cache->v),
+        (int64_t)(cache->num_blocks * 16), (int64_t)(cache->block_stride / 8), (int64_t)(cache->token_stride / 8),
+        (int64_t)(cache->head_stride / 8), c.slot_mapping, err);
     snprintf(info, info_len, "reshape_and_cache tokens=%lld grid=%lld block=256", (long long)c.num_tokens,
              (long long)blocks);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(e);
 }
 
 // Validates an attention call and fills the kernel arguments and the plan.

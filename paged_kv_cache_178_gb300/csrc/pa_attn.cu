@@ -456,6 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // waits just before its first K/V copy.
     if (!p.early_reads)
         griddep_wait();
+    // a grid launched after this one with programmatic serialization may be
+    // scheduled now (it waits for this grid before it reads our results)
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by indexing the shared array so the
     // compiler keeps every access in the shared state space

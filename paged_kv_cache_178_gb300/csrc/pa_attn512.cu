@@ -59,6 +59,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     // launched with programmatic stream serialization: no global read before
     // the preceding grid of the stream has completed
     griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sK = smem;

@@ -88,6 +88,10 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 // Wait until the preceding grid of the stream has completed and its memory
 // operations are visible; returns at once when there is no such dependency.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ------------------------------------------------------------- tcgen05 ----
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
