@@ -150,19 +150,35 @@ __device__ __forceinline__ void acc_row_store(float4 *acc, int r, int g, const u
                                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
 }
 
-// Arrival on the (request, KV head, query tile) counter; the last CTA to
-// arrive folds the chunk partial states left to right and writes out / lse
-// (C5, C6).  All threads of the CTA take part; `work` is shared memory the
-// pipeline no longer uses.  The fold is staged: a segment of records is
+// Arrival on the (request, KV head, query tile) counter and the fold of the
+// chunk partial states, left to right (C5, C6).  All threads of the CTA take
+// part; `work` is shared memory the pipeline no longer uses.
+//
+// With `multi` (every unit of the grid is resident at once: units <= SMs, one
+// CTA per SM) the last kMergers CTAs to arrive share the fold: CTA m of them
+// folds columns [m*DH/K, (m+1)*DH/K) of every row.  Each first waits (bounded)
+// until the whole group has arrived; they are the only CTAs that wait, and
+// every CTA they wait for already holds an SM.  Otherwise the last CTA to
+// arrive folds every column.  The fold is staged: a segment of records is
 // copied to shared memory in one pass, the per-row coefficient chain
 // (fold_coef) runs once per row, then every element applies fold_elem in
 // chunk order -- the same operations, in the same order, as the in-CTA fold.
+constexpr int kMergers = 4;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *ptr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 template <int DH>
 __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int nchunks, int rv,
                                        int64_t tok_first, int kvh, float *work, int work_floats,
-                                       int *flag_last)
+                                       int *flag_merger, bool multi)
 {
     const int tid = threadIdx.x, nth = blockDim.x;
+    const int K = (multi && nchunks >= kMergers) ? kMergers : 1;
     if (tid == 0) {
         // acquire-release at GPU scope: releases this CTA's partial record
         // (written before the CTA barrier that precedes this call) and, for
@@ -172,26 +188,55 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
                      : "=r"(old)
                      : "l"(p.ws_cnt + unit_q)
                      : "memory");
-        const int last = (old == (uint32_t)(nchunks - 1));
-        if (last)
+        int merger = (int)old - (nchunks - K);  // < 0: not one of the last K
+        if (merger >= K)
+            merger = -1;  // a counter left over by a failed call: fold nothing
+        if (merger >= 0 && K > 1) {
+            // wait for the rest of the group: once the counter reaches
+            // nchunks every partial record is visible (the acquire reads the
+            // end of the release sequence formed by the arrivals)
+            if (merger < K - 1) {
+                const uint64_t t0 = global_timer_ns();
+                while (ld_acquire_u32(p.ws_cnt + unit_q) < (uint32_t)nchunks) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        record_error(p.err, kErrTimeout, ((long long)blockIdx.x << 8) | 0xFF);
+                        merger = -1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            // leave: the last of the K to pass its wait returns the counter
+            // to zero for the next call (no CTA reads it after that)
+            if (merger >= 0) {
+                const uint32_t left = atomicAdd(p.ws_cnt + unit_q, 1u);
+                if (left == (uint32_t)(nchunks + K - 1))
+                    atomicExch(p.ws_cnt + unit_q, 0u);
+            }
+        } else if (merger >= 0) {
             p.ws_cnt[unit_q] = 0u;  // leave the workspace ready for the next call
-        *flag_last = last;
+        }
+        *flag_merger = merger;
     }
     __syncthreads();
-    if (!*flag_last)
+    const int merger = *flag_merger;
+    if (merger < 0)
         return;
+    constexpr int kColsAll = DH;
+    const int ncol = kColsAll / K;   // columns this CTA folds
+    const int col0 = merger * ncol;
     const int R = p.ws_rows;
     const int64_t hdr = part_header_floats(R);
     const int64_t ustride = part_record_floats(R, DH);
     const float *part0 = p.ws_part + unit_q * p.nch * ustride;
     const int run_f = (2 * rv + 3) / 4 * 4;
-    float *s_acc = work;                 // [rv][DH] running O
-    float *s_run = s_acc + rv * DH;      // [rv][2] running (m, l)
+    float *s_acc = work;                 // [rv][ncol] running O (this CTA's columns)
+    float *s_run = s_acc + rv * ncol;    // [rv][2] running (m, l)
     float *s_run2 = s_run + run_f;       // [rv][2] (m, l) after the current segment
     float *s_seg = s_run2 + run_f;
-    const int per_chunk = rv * (DH + 5) + 8;
-    const int seg = max(1, (work_floats - rv * DH - 2 * run_f) / per_chunk);
-    for (int e = tid; e < rv * DH; e += nth)
+    const int per_chunk = rv * (ncol + 5) + 8;
+    const int seg = max(1, (work_floats - rv * ncol - 2 * run_f) / per_chunk);
+    for (int e = tid; e < rv * ncol; e += nth)
         s_acc[e] = 0.f;
     for (int r = tid; r < rv; r += nth) {
         s_run[2 * r] = -INFINITY;
@@ -200,8 +245,8 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
     for (int c0 = 0; c0 < nchunks; c0 += seg) {
         const int cn = min(seg, nchunks - c0);
         float *s_ml = s_seg;                             // [cn][rv][2]
-        float *s_o = s_ml + (2 * cn * rv + 3) / 4 * 4;   // [cn][rv][DH]
-        float *s_cf = s_o + cn * rv * DH;                // [cn][rv][2]
+        float *s_o = s_ml + (2 * cn * rv + 3) / 4 * 4;   // [cn][rv][ncol]
+        float *s_cf = s_o + cn * rv * ncol;              // [cn][rv][2]
         int *s_md = reinterpret_cast<int *>(s_cf + 2 * cn * rv);  // [cn][rv]
         // (a) stage the segment's records: every copy in flight at once
         for (int i = tid; i < cn * rv * 2; i += nth) {
@@ -211,11 +256,14 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
                          "l"(part0 + (c0 + c) * ustride + which * R + r)
                          : "memory");
         }
-        const int vec_per_chunk = rv * DH / 4;
+        const int vec_per_row = ncol / 4;
+        const int vec_per_chunk = rv * vec_per_row;
         for (int i = tid; i < cn * vec_per_chunk; i += nth) {
             const int c = i / vec_per_chunk, k = i % vec_per_chunk;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(s_o + c * rv * DH + 4 * k)),
-                         "l"(part0 + (c0 + c) * ustride + hdr + 4 * k)
+            const int r = k / vec_per_row, v4 = k % vec_per_row;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             smem_addr(s_o + (c * rv + r) * ncol + 4 * v4)),
+                         "l"(part0 + (c0 + c) * ustride + hdr + (int64_t)r * DH + col0 + 4 * v4)
                          : "memory");
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -237,52 +285,59 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
         }
         __syncthreads();
         // (c) the sequential parts, in chunk order -- the same operations
-        //     fold_coef / fold_elem perform: (m, l) per row on its own thread,
-        //     O per element, with no branch inside the element chain
-        // (loads first, selects after: only the arithmetic is serial)
-        for (int r = tid; r < rv; r += nth) {
-            float ma = s_run[2 * r], la = s_run[2 * r + 1];
-#pragma unroll 4
-            for (int c = 0; c < cn; ++c) {
-                const int md = s_md[c * rv + r];
-                const float2 ml = *reinterpret_cast<const float2 *>(s_ml + (c * rv + r) * 2);
-                const float2 cf = *reinterpret_cast<const float2 *>(s_cf + (c * rv + r) * 2);
-                const float l2 = __fadd_rn(__fmul_rn(la, cf.x), __fmul_rn(ml.y, cf.y));
-                const float m2 = fmaxf(ma, ml.x);
-                la = md == 1 ? ml.y : (md == 2 ? l2 : la);
-                ma = md == 1 ? ml.x : (md == 2 ? m2 : ma);
-            }
-            s_run2[2 * r] = ma;
-            s_run2[2 * r + 1] = la;
-        }
-        // four consecutive elements of one row per thread: one 16-byte load
-        // per chunk, the row's coefficients shared; operands of seven chunks
-        // are loaded before their seven fold steps
-        for (int e4 = tid; e4 < rv * DH / 4; e4 += nth) {
-            const int e = e4 * 4, r = e / DH;
-            float4 oa = *reinterpret_cast<const float4 *>(s_acc + e);
-            for (int cb = 0; cb < cn; cb += 7) {
-                float4 o7[7];
-                float a7[7], b7[7];
-                int m7[7];
+        //     fold_coef / fold_elem perform, with no branch inside a chain.
+        //     The (m, l) chains run on the last warps, one row per thread;
+        //     the O chains on the others, one element per thread and pass.
+        //     Each loads the operands of seven chunks before their seven steps.
+        const int n_ml = (rv + 31) / 32 * 32;
+        const int n_o = nth - n_ml;
+        if (tid >= n_o) {
+            const int r = tid - n_o;
+            if (r < rv) {
+                float ma = s_run[2 * r], la = s_run[2 * r + 1];
+                for (int cb = 0; cb < cn; cb += 7) {
+                    int md7[7];
+                    float2 ml7[7], cf7[7];
 #pragma unroll
-                for (int k = 0; k < 7; ++k) {
-                    const int c = min(cb + k, cn - 1);
-                    o7[k] = *reinterpret_cast<const float4 *>(s_o + c * rv * DH + e);
-                    const float2 cf = *reinterpret_cast<const float2 *>(s_cf + (c * rv + r) * 2);
-                    a7[k] = cf.x;
-                    b7[k] = cf.y;
-                    m7[k] = cb + k < cn ? s_md[c * rv + r] : 0;  // past the last chunk: keep
-                }
+                    for (int k = 0; k < 7; ++k) {
+                        const int c = min(cb + k, cn - 1);
+                        md7[k] = cb + k < cn ? s_md[c * rv + r] : 0;  // past the last chunk: keep
+                        ml7[k] = *reinterpret_cast<const float2 *>(s_ml + (c * rv + r) * 2);
+                        cf7[k] = *reinterpret_cast<const float2 *>(s_cf + (c * rv + r) * 2);
+                    }
 #pragma unroll
-                for (int k = 0; k < 7; ++k) {
-                    oa.x = fold_elem_sel(oa.x, o7[k].x, a7[k], b7[k], m7[k]);
-                    oa.y = fold_elem_sel(oa.y, o7[k].y, a7[k], b7[k], m7[k]);
-                    oa.z = fold_elem_sel(oa.z, o7[k].z, a7[k], b7[k], m7[k]);
-                    oa.w = fold_elem_sel(oa.w, o7[k].w, a7[k], b7[k], m7[k]);
+                    for (int k = 0; k < 7; ++k) {
+                        const float l2 = __fadd_rn(__fmul_rn(la, cf7[k].x), __fmul_rn(ml7[k].y, cf7[k].y));
+                        const float m2 = fmaxf(ma, ml7[k].x);
+                        la = md7[k] == 1 ? ml7[k].y : (md7[k] == 2 ? l2 : la);
+                        ma = md7[k] == 1 ? ml7[k].x : (md7[k] == 2 ? m2 : ma);
+                    }
                 }
+                s_run2[2 * r] = ma;
+                s_run2[2 * r + 1] = la;
             }
-            *reinterpret_cast<float4 *>(s_acc + e) = oa;
+        } else {
+            for (int e = tid; e < rv * ncol; e += n_o) {
+                const int r = e / ncol;
+                float oa = s_acc[e];
+                for (int cb = 0; cb < cn; cb += 7) {
+                    float o7[7], a7[7], b7[7];
+                    int m7[7];
+#pragma unroll
+                    for (int k = 0; k < 7; ++k) {
+                        const int c = min(cb + k, cn - 1);
+                        o7[k] = s_o[c * rv * ncol + e];
+                        const float2 cf = *reinterpret_cast<const float2 *>(s_cf + (c * rv + r) * 2);
+                        a7[k] = cf.x;
+                        b7[k] = cf.y;
+                        m7[k] = cb + k < cn ? s_md[c * rv + r] : 0;  // past the last chunk: keep
+                    }
+#pragma unroll
+                    for (int k = 0; k < 7; ++k)
+                        oa = fold_elem_sel(oa, o7[k], a7[k], b7[k], m7[k]);
+                }
+                s_acc[e] = oa;
+            }
         }
         __syncthreads();
         for (int r = tid; r < rv; r += nth) {
@@ -293,8 +348,8 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
     }
     // (d) epilogue
     const int G = p.group;
-    for (int e = tid; e < rv * DH; e += nth) {
-        const int r = e / DH, d = e % DH;
+    for (int e = tid; e < rv * ncol; e += nth) {
+        const int r = e / ncol, d = col0 + e % ncol;
         const float ma = s_run[2 * r], la = s_run[2 * r + 1];
         const int64_t t = tok_first + r / G;
         const int h = kvh * G + r % G;
@@ -314,6 +369,7 @@ __device__ __forceinline__ int tile_chunks(const ReqMeta &m, int qt, int tq, int
 
 struct Unit {
     int b, kvh, qt, c;
+    int total;  // units in the whole grid (every CTA computes the same count)
     bool valid;  // false: this CTA has nothing to do
     ReqMeta meta;
 };
@@ -356,6 +412,9 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
     if (tid == 0)
         s_int[32] = -1;
     __syncthreads();
+    int total = 0;
+    for (int w = 0; w < (int)(blockDim.x / 32); ++w)
+        total += s_int[w];
     int wpre = 0;
     for (int w = 0; w < warp; ++w)
         wpre += s_int[w];
@@ -373,6 +432,7 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
     __syncthreads();
     Unit u;
     u.valid = false;
+    u.total = total;
     const int b = s_int[32];
     if (b < 0)
         return u;
@@ -488,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
     // ---------------------------------------------------------- work unit --
     int b, kvh, qt, c_grid = 0;
+    bool split_multi = false;  // the last arrivals share the fold (all units resident)
     ReqMeta meta;
     if (p.split) {
         const Unit un = split_unit(p, CHUNK_DIV, reinterpret_cast<int *>(s_x));
@@ -498,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         qt = un.qt;
         c_grid = un.c;
         meta = un.meta;
+        split_multi = un.total <= p.num_sms;
     } else {
         // longest work first: later query tiles see more keys.  With cl = 2
         // the CTA pair takes query tiles 2g and 2g+1 of one (request, KV head).
@@ -1196,7 +1258,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }  // no CTA leaves while its partner may still write into it
     if (p.split)
         split_arrive_and_merge<DH>(p, unit_q, nchunks, rows_valid, tok_first, kvh, merge_work,
-                                   kMergeWorkFloats, &sflags[2]);
+                                   kMergeWorkFloats, &sflags[2], split_multi);
 }
 
 // ------------------------------------------------------------------ host --
@@ -1254,6 +1316,22 @@ cudaError_t init_attention_attributes()
     return init_attention512_attributes();
 }
 
+// SM count of the current device, looked up once per device.
+static int num_sms_of_current_device()
+{
+    static int cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;  // 0: the fold is never shared
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 template <int DH>
 static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *err, cudaStream_t stream)
 {
@@ -1304,6 +1382,7 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.ws_rows = pl.ws_rows;
     p.split = pl.split ? 1 : 0;
     p.npairs = (pl.qtiles + 1) / 2;
+    p.num_sms = num_sms_of_current_device();
     p.early_reads = a.early_reads ? 1 : 0;
     // C2: scale * log2(e) formed once, in fp32, on the host
     p.scale_log2 = a.scale * 1.4426950408889634f;
