@@ -218,6 +218,31 @@ def test_batch_composition_and_order_do_not_change_bits():
         _bitwise(lse[b:b + 1], l1, f"request {b} alone (lse)")
 
 
+def test_shared_fold_equals_single_fold():
+    """Split-KV decode: when every unit of the grid is resident at once, the
+    last four arrivals of a (request, KV head) group share the chunk fold by
+    columns; in a grid with more units than SMs the last arrival folds alone.
+    A request's bits must not depend on which of the two ran."""
+    lens = [7168] + [1024] * 40
+    w = wl.decode(seq_lens=lens, num_blocks=4096)
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = 2 * sum((L + 255) // 256 for L in lens)
+    assert units > n_sms  # the whole batch folds with one CTA per group
+    dw, out, lse = _run(w)
+    assert "split" in pagedattn.last_launch_info()
+    dev = out.device
+    o1, l1 = dw.attention(q=dw.q[0:1], block_tables=dw.block_tables[0:1].contiguous(),
+                          seq_lens=dw.seq_lens[0:1].contiguous(),
+                          query_start_loc=torch.tensor([0, 1], dtype=torch.int32, device=dev),
+                          max_seq_len=7168)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    assert "split" in pagedattn.last_launch_info()
+    assert 2 * 28 <= n_sms  # request 0 alone: 56 units, the fold is shared
+    _bitwise(out[0:1], o1, "request 0: single-CTA fold vs shared fold")
+    _bitwise(lse[0:1], l1, "request 0 lse: single-CTA fold vs shared fold")
+    _compare(w, out, lse, rows=[0, 1, 17, 40], tag=" (41 requests)")
+
+
 def test_prefill_bounds_and_schedule_switch():
     """The same prefill rows through in-CTA and split-KV schedules (the
     schedule follows host bounds only) stay bit-identical."""
