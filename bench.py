@@ -410,6 +410,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
     }
     if not args.no_secondary:
+        line["decode_scaled"] = measure_decode_scaled(args, dev, stream, ws, peaks, peak_src)
         line["prefill"] = measure_prefill(args, dev, stream, ws, peaks, peak_src)
         line["prefill_wide"] = measure_prefill(args, dev, stream, ws, peaks, peak_src, launches=20,
                                                wide=True)
@@ -456,6 +457,40 @@ def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200,
             "us_per_launch": round(t * 1e6, 2), "flops_per_launch": flops,
             "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4),
             "peak_source": f"{peak_src} bf16_tflops (burst)", "schedule": info}
+
+
+def measure_decode_scaled(args, dev, stream, ws, peaks, peak_src, copies: int = 16, launches: int = 50):
+    """The decode length mix repeated `copies` times (B = 4*copies requests,
+    the same Hq/Hkv/Dh and page size): attention launches alone, K/V bytes of
+    valid tokens per launch over the launch time.  With 16 copies a launch
+    reads 312 MB, more than twice the L2, so it reads from HBM."""
+    from paged_kv_cache_178_gb300 import pagedattn
+    from paged_kv_cache_178_gb300.device import DeviceWorkload
+    lens = list(wl.DECODE_LENS) * copies
+    total_pages = sum(wl.pages_needed(L) for L in lens)
+    w = wl.decode(seq_lens=lens, num_blocks=total_pages + 64)
+    dw = DeviceWorkload(w, device=str(dev), fill_bits=None)
+    dw.write_cache()
+    out = torch.empty_like(dw.q)
+    lse = torch.empty(dw.q.shape[:2], dtype=torch.float32, device=dev)
+
+    def attn(i):
+        dw.attention(out=out, lse=lse)
+
+    with torch.cuda.stream(stream):
+        attn(0)
+    torch.cuda.synchronize()
+    info = pagedattn.last_launch_info()
+    g = GraphedSteps(attn, 1, stream, chunk=50)
+    g.prepare(launches)
+    g.run(4)
+    t = time_graphed(g, launches, stream, ws) / launches
+    nbytes = attn_io_bytes(w)
+    gbs = nbytes / t / 1e9
+    return {"workload": f"decode B={len(lens)} (the B=4 length mix x{copies}) Q=1 Hq=8 Hkv=2 Dh=128",
+            "gbs": round(gbs, 1), "us_per_launch": round(t * 1e6, 2), "bytes_per_launch": nbytes,
+            "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_source": f"{peak_src} hbm_gbs", "schedule": info}
 
 
 def _packed(tensors, device=None, pin=False):

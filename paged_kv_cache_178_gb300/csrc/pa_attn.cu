@@ -173,12 +173,14 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *ptr)
 }
 
 template <int DH>
-__device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int nchunks, int rv,
-                                       int64_t tok_first, int kvh, float *work, int work_floats,
-                                       int *flag_merger, bool multi)
+__device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int64_t unit_q, int nchunks,
+                                       int narrive, int rv, int64_t tok_first, int kvh, float *work,
+                                       int work_floats, int *flag_merger, bool multi)
 {
+    // narrive: CTAs of the group (each brings ceil-divided consecutive
+    // chunks); nchunks: chunk records to fold
     const int tid = threadIdx.x, nth = blockDim.x;
-    const int K = (multi && nchunks >= kMergers) ? kMergers : 1;
+    const int K = (multi && narrive >= kMergers) ? kMergers : 1;
     if (tid == 0) {
         // acquire-release at GPU scope: releases this CTA's partial record
         // (written before the CTA barrier that precedes this call) and, for
@@ -188,16 +190,16 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
                      : "=r"(old)
                      : "l"(p.ws_cnt + unit_q)
                      : "memory");
-        int merger = (int)old - (nchunks - K);  // < 0: not one of the last K
+        int merger = (int)old - (narrive - K);  // < 0: not one of the last K
         if (merger >= K)
             merger = -1;  // a counter left over by a failed call: fold nothing
         if (merger >= 0 && K > 1) {
             // wait for the rest of the group: once the counter reaches
-            // nchunks every partial record is visible (the acquire reads the
+            // narrive every partial record is visible (the acquire reads the
             // end of the release sequence formed by the arrivals)
             if (merger < K - 1) {
                 const uint64_t t0 = global_timer_ns();
-                while (ld_acquire_u32(p.ws_cnt + unit_q) < (uint32_t)nchunks) {
+                while (ld_acquire_u32(p.ws_cnt + unit_q) < (uint32_t)narrive) {
                     if (global_timer_ns() - t0 > kWaitLimitNs) {
                         record_error(p.err, kErrTimeout, ((long long)blockIdx.x << 8) | 0xFF);
                         merger = -1;
@@ -210,7 +212,7 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
             // to zero for the next call (no CTA reads it after that)
             if (merger >= 0) {
                 const uint32_t left = atomicAdd(p.ws_cnt + unit_q, 1u);
-                if (left == (uint32_t)(nchunks + K - 1))
+                if (left == (uint32_t)(narrive + K - 1))
                     atomicExch(p.ws_cnt + unit_q, 0u);
             }
         } else if (merger >= 0) {
@@ -394,7 +396,7 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
                 cnt = qtl;
             } else {
                 for (int qt = 0; qt < qtl; ++qt)
-                    cnt += tile_chunks(m, qt, p.tq, chunk);
+                    cnt += (tile_chunks(m, qt, p.tq, chunk) + p.cpu - 1) / p.cpu;
             }
             cnt *= p.hkv;
         }
@@ -455,11 +457,11 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
     }
     int per_kvh = 0;
     for (int qt = 0; qt < qtl; ++qt)
-        per_kvh += tile_chunks(m, qt, p.tq, chunk);
+        per_kvh += (tile_chunks(m, qt, p.tq, chunk) + p.cpu - 1) / p.cpu;
     u.kvh = r / per_kvh;
     r %= per_kvh;
     for (int qt = 0; qt < qtl; ++qt) {
-        const int n = tile_chunks(m, qt, p.tq, chunk);
+        const int n = (tile_chunks(m, qt, p.tq, chunk) + p.cpu - 1) / p.cpu;
         if (r < n) {
             u.qt = qt;
             u.c = r;
@@ -594,8 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int nchunks = CHUNKED ? (kend + CHUNK_DIV - 1) / CHUNK_DIV : 1;
     int kbeg = 0, kstop = kend;
     if (p.split) {
-        kbeg = c_grid * CHUNK_DIV;
-        kstop = min(kbeg + CHUNK_DIV, kend);
+        // this CTA's consecutive chunks [c_grid*cpu, c_grid*cpu + cpu)
+        kbeg = c_grid * p.cpu * CHUNK_DIV;
+        kstop = min(kbeg + p.cpu * CHUNK_DIV, kend);
     }
     const int t_begin = kbeg / kKeys;
     const int t_end = (kstop + kKeys - 1) / kKeys;
@@ -1153,8 +1156,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             const float l = s_ml[((k & 1) * kRows + r) * 2 + 1];
             const bool bad = final_chunk && sflags[3] != 0;
             if (p.split) {
-                // partial state of this CTA's chunk: m, l and the O row
-                float *part = p.ws_part + (unit_q * p.nch + c_grid) * rec_floats;
+                // partial state of chunk c_grid*cpu + k: m, l and the O row
+                float *part = p.ws_part + (unit_q * p.nch + (int64_t)c_grid * p.cpu + k) * rec_floats;
                 const float qnan = __int_as_float(0x7FC00000);
                 if (row_valid) {
                     part[r] = bad ? 0.f : m;
@@ -1257,8 +1260,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             tmem_dealloc(tmem, 512);
     }  // no CTA leaves while its partner may still write into it
     if (p.split)
-        split_arrive_and_merge<DH>(p, unit_q, nchunks, rows_valid, tok_first, kvh, merge_work,
-                                   kMergeWorkFloats, &sflags[2], split_multi);
+        split_arrive_and_merge<DH>(p, unit_q, nchunks, (nchunks + p.cpu - 1) / p.cpu, rows_valid, tok_first,
+                                   kvh, merge_work, kMergeWorkFloats, &sflags[2], split_multi);
 }
 
 // ------------------------------------------------------------------ host --
@@ -1283,6 +1286,16 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     const long long full_ctas = (long long)num_seqs * num_kv_heads * pl.qtiles;
     pl.split = chunk > 0 && max_seq_len > chunk && full_ctas < kSplitCtaThreshold;
     pl.nch = pl.split ? (max_seq_len + chunk - 1) / chunk : 1;
+    // Split-KV: about four waves of CTAs at most.  Larger batches give each CTA
+    // several consecutive chunks (still one record per chunk, so the fold and
+    // the results are the same whatever cpu is).
+    pl.cpu = 1;
+    if (pl.split) {
+        const long long target = 4LL * kSplitCtaThreshold;
+        const long long units = full_ctas * pl.nch;
+        if (units > target)
+            pl.cpu = (int)((units + target - 1) / target);
+    }
     pl.ws_rows = G * (max_query_len < pl.tokens_per_tile ? max_query_len : pl.tokens_per_tile);
     pl.ws_counter_bytes = 0;
     pl.ws_bytes = 0;
@@ -1295,7 +1308,8 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     // (head dims 128/256)
     pl.cl = (!pl.split && head_dim != 512 && pl.qtiles >= 2) ? 2 : 1;
     const long long qgroups = pl.cl == 2 ? (pl.qtiles + 1) / 2 * 2 : pl.qtiles;
-    pl.grid = (long long)num_seqs * num_kv_heads * qgroups * pl.nch * (head_dim == 512 ? 2 : 1);
+    pl.grid = (long long)num_seqs * num_kv_heads * qgroups * ((pl.nch + pl.cpu - 1) / pl.cpu) *
+              (head_dim == 512 ? 2 : 1);
     *plan = pl;
     return true;
 }
@@ -1383,6 +1397,7 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.split = pl.split ? 1 : 0;
     p.npairs = (pl.qtiles + 1) / 2;
     p.num_sms = num_sms_of_current_device();
+    p.cpu = pl.cpu;
     p.early_reads = a.early_reads ? 1 : 0;
     // C2: scale * log2(e) formed once, in fp32, on the host
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -1411,11 +1426,12 @@ cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &pl, ErrState *er
                              char *info, size_t info_len)
 {
     if (info && info_len)
-        snprintf(info, info_len, "attention dh=%d schedule=%s grid=%lld qtiles=%d chunks=%d kv_tile=%d chunk=%d",
+        snprintf(info, info_len, "attention dh=%d schedule=%s grid=%lld qtiles=%d chunks=%d kv_tile=%d chunk=%d cpu=%d",
                  pl.head_dim,
                  pl.split ? "split-kv" : (pl.head_dim == 512 ? "in-cta-pair" : (pl.cl == 2 ? "in-cta-pair2sm" : "in-cta")),
                  pl.grid,
-                 pl.qtiles, pl.nch, pl.head_dim == 512 ? 64 : kKeys, pl.head_dim == 128 ? Cfg<128>::kChunk : 0);
+                 pl.qtiles, pl.nch, pl.head_dim == 512 ? 64 : kKeys, pl.head_dim == 128 ? Cfg<128>::kChunk : 0,
+                 pl.cpu);
     if (pl.grid == 0)
         return cudaSuccess;
     switch (a.head_dim) {

@@ -39,6 +39,7 @@ struct AttnParams {
     int32_t npairs;  // query-tile pairs (in-CTA schedule on CTA pairs)
     int32_t early_reads;  // only the K/V copies wait for the preceding grid
     int32_t num_sms;      // SMs of the device (split-KV: whether every unit is resident)
+    int32_t cpu;          // split-KV: consecutive chunks per CTA (each still writes one record per chunk)
     float scale_log2;
 };
 

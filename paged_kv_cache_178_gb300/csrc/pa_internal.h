@@ -61,6 +61,7 @@ struct AttnPlan {
     int qtiles;         // grid extent over query tiles
     int nch;            // grid extent over KV chunks (1 unless split)
     bool split;         // split-KV with partial states + in-kernel merge
+    int cpu;            // split-KV: consecutive chunks per CTA (>= 1)
     int cl;             // CTAs per cluster multicasting K/V tiles (in-CTA schedule)
     int ws_rows;        // rows per partial-state record
     size_t ws_counter_bytes;
