@@ -159,8 +159,10 @@ PA_API size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_
  *   workspace         : device scratch of at least
  *                       pa_paged_attention_workspace_size(...) bytes, 256-byte
  *                       aligned, zero-filled before its first use; the library
- *                       leaves it ready for the next call.  One workspace must
- *                       not be used by two calls that may run concurrently.
+ *                       leaves it ready for the next call (after a call that
+ *                       reports PA_ERR_TIMEOUT, zero-fill it again).  One
+ *                       workspace must not be used by two calls that may run
+ *                       concurrently.
  * Supported: head_dim in {128, 256, 512}; Hq % Hkv == 0; Hq/Hkv <= 128.
  *
  * Arithmetic is fixed ([R] intro: one schedule for strict agreement): every
