@@ -141,6 +141,39 @@ def test_mixed_batch_small_dims():
     _compare(w, out, lse)
 
 
+@pytest.mark.parametrize("hq,hkv,dh", [(2, 2, 128), (6, 2, 128), (32, 2, 128), (128, 1, 128),
+                                        (12, 4, 256)])
+def test_group_sizes(hq, hkv, dh):
+    """Query-head groups G = Hq/Hkv from 1 (one KV head per query head) to
+    128 (one token per 128-row tile), and a G that does not divide 128 (rows
+    of a tile left unused), on a batch mixing prefill, suffix and decode; the
+    prefill rows of one request equal its decode view bit for bit."""
+    gen = torch.Generator().manual_seed(40 + hq)
+    lens = [300, 700, 1, 513, 40]
+    qlens = [300, 9, 1, 1, 40]
+    nb = sum(wl.pages_needed(L) for L in lens) + 8
+    pages = torch.randperm(nb, generator=gen).tolist()
+    rows, at = [], 0
+    for L in lens:
+        n = wl.pages_needed(L)
+        rows.append(pages[at:at + n])
+        at += n
+    w = wl.build(f"groups_hq{hq}_hkv{hkv}_dh{dh}", num_q_heads=hq, num_kv_heads=hkv, head_dim=dh,
+                 seq_lens=lens, query_lens=qlens, num_blocks=nb, block_rows=rows, layout="separate",
+                 seed=41 + hq)
+    dw, out, lse = _run(w)
+    _compare(w, out, lse)
+    # request 4 (a 40-token prefill) against its decode view
+    q0, q1 = int(w.query_start_loc[4]), int(w.query_start_loc[5])
+    kv0 = sum(lens[:4])
+    wb = wl.Workload(name=w.name + "_r4", num_q_heads=hq, num_kv_heads=hkv, head_dim=dh, num_blocks=nb,
+                     layout=w.layout, q=w.q[q0:q1], key=w.key[kv0:kv0 + 40], value=w.value[kv0:kv0 + 40],
+                     slot_mapping=w.slot_mapping[kv0:kv0 + 40], block_table=w.block_table[4:5],
+                     seq_lens=w.seq_lens[4:5], query_start_loc=torch.tensor([0, 40], dtype=torch.int32),
+                     scale=w.scale)
+    _prefill_vs_decode(wb, list(range(40)))
+
+
 # ------------------------------------------------ prefill == decode bitwise ----
 
 def _prefill_vs_decode(w, rows):
