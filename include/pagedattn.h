@@ -241,6 +241,51 @@ PA_API pa_status pa_reshape_and_paged_attention(
     size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Compact active-block gather of one KV head ("ROCm: harden compact
+ * peer-local KV prefill for Gemma-4", Scope and Required hardening: the
+ * block-table-selected pages of one K/V head packed for transfer, with
+ * shuffled and sparse blocks, page boundaries, invalid metadata and byte
+ * budgets).  Request b with L_b = seq_lens[b] tokens selects the
+ * n_b = ceil(L_b / 16) pages block_tables[b][0..n_b-1].  With
+ * off_b = n_0 + ... + n_{b-1} and total = off_{num_seqs}:
+ *   packed_k[off_b + p][t][:] = K[block_tables[b][p]][t][kv_head][:]
+ *   packed_v[off_b + p][t][:] = V[block_tables[b][p]][t][kv_head][:]
+ *   compact_tables[b][p]      = off_b + p for p < n_b, -1 for p >= n_b
+ *   compact_offsets[b]        = off_b, compact_offsets[num_seqs] = total
+ * Whole pages are copied (a partial last page carries its tail rows as they
+ * are in the pool).  The packed buffers form a pool of their own with one KV
+ * head ({k, v, capacity_pages, 16, 1, Dh, 0, 16*Dh, Dh, Dh}); attention over
+ * it with compact_tables and the group's query heads gives the same bits as
+ * attention over the full pool.
+ *   cache             : the pool (read only).  kv_head in [0, Hkv).
+ *   block_tables      : [num_seqs, max_blocks_per_seq] int32, seq_lens
+ *                       [num_seqs] int32, both on the device.
+ *   packed_k, packed_v: [capacity_pages, 16, Dh] BF16 each, contiguous,
+ *                       16-byte aligned, caller-owned (may be NULL when
+ *                       capacity_pages == 0).
+ *   compact_tables    : [num_seqs, max_blocks_per_seq] int32 (written).
+ *   compact_offsets   : [num_seqs + 1] int32 (written).
+ * Errors latched on the device and read with pa_check_errors:
+ *   - a length outside [0, max_blocks_per_seq*16]: that request gets no
+ *     pages; PA_ERR_BAD_METADATA, index = the request;
+ *   - a block id outside [0, num_blocks): that packed page is NaN;
+ *     PA_ERR_BAD_METADATA, index = the request;
+ *   - total > capacity_pages: only compact_offsets is written (so the caller
+ *     learns the size it needs); PA_ERR_WORKSPACE, index = total.
+ * Host errors: PA_ERR_INVALID_ARG (bad head, sizes or pointers, or an
+ * output that shares bytes with the pool, block_tables, seq_lens or another
+ * output),
+ * PA_ERR_UNSUPPORTED (num_seqs > 512 or num_seqs*max_blocks_per_seq >
+ * INT32_MAX).  num_seqs == 0 launches nothing.  The launch waits for the
+ * work before it on the stream (it may be launched early with programmatic
+ * stream serialization and waits in the kernel).
+ */
+PA_API pa_status pa_gather_kv_head(const pa_kv_cache *cache, int32_t kv_head, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                   void *packed_k, void *packed_v, int64_t capacity_pages,
+                                   int32_t *compact_tables, int32_t *compact_offsets, pa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * flag.  Returns PA_OK, PA_ERR_BAD_METADATA or PA_ERR_TIMEOUT (or
  * PA_ERR_CUDA if the synchronisation failed).  *first_bad_index (may be

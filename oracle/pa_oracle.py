@@ -12,6 +12,10 @@ depends on the CUDA library or on torch's BF16 arithmetic.
                         table ("stabilize direct paged CK attention for bitwise
                         R/R", Additional checks: full/suffix execution,
                         causal/LSE vs decode)
+  gather_kv_head     -- the block-table-selected pages of one KV head packed
+                        in request order, with compact table and offsets
+                        ("ROCm: harden compact peer-local KV prefill for
+                        Gemma-4", Scope and Required hardening)
 """
 from __future__ import annotations
 
@@ -153,3 +157,75 @@ def paged_attention(q_bits: np.ndarray, pool: HostPool, block_tables: np.ndarray
         0 if rows_arr is None else _ptr(rows_arr), nrows, _ptr(out), _ptr(lse),
         int(num_threads))
     return out, lse
+
+
+NAN_BITS = 0x7FC0  # BF16 quiet NaN written for a page whose block id is bad
+
+
+class Gathered:
+    """Result of gather_kv_head: packed K/V [total, 16, Dh] bit patterns (None
+    when over budget), compact table [B, max_blocks] (None when over budget),
+    offsets [B + 1], the requests with bad metadata (ascending) and, when
+    over budget, the pages needed (else None)."""
+
+    def __init__(self, packed_k, packed_v, compact_tables, offsets, bad_requests, budget_needed):
+        self.packed_k, self.packed_v = packed_k, packed_v
+        self.compact_tables, self.offsets = compact_tables, offsets
+        self.bad_requests, self.budget_needed = bad_requests, budget_needed
+
+
+def gather_kv_head(pool: HostPool, kv_head: int, block_tables: np.ndarray, seq_lens: np.ndarray,
+                   capacity_pages: int) -> Gathered:
+    """Pack the pages that request b selects -- block_tables[b][p] for
+    p < ceil(L_b / 16) -- of head kv_head, request after request, page after
+    page ("ROCm: harden compact peer-local KV prefill for Gemma-4", Scope:
+    compact active block-table-selected K/V head).  Hardening, same source:
+    a length outside [0, 16 * max_blocks] selects no page and marks its
+    request bad; a block id outside the pool gives a NaN page and marks its
+    request bad; more pages than capacity_pages writes the offsets only and
+    reports the pages needed."""
+    bt = np.asarray(block_tables, dtype=np.int64)
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    num_seqs, max_blocks = bt.shape
+    bad = set()
+    pages = []
+    for b, L in enumerate(lens):
+        if L < 0 or L > BLOCK_SIZE * max_blocks:
+            bad.add(b)
+            pages.append(0)
+        else:
+            pages.append(-(-L // BLOCK_SIZE))
+    offsets = np.zeros(num_seqs + 1, dtype=np.int64)
+    for b in range(num_seqs):
+        offsets[b + 1] = offsets[b] + pages[b]
+    total = int(offsets[num_seqs])
+    if total > capacity_pages:
+        return Gathered(None, None, None, offsets, sorted(bad), total)
+    compact = np.full((num_seqs, max_blocks), -1, dtype=np.int64)
+    dh = pool.head_dim
+    packed_k = np.zeros((total, BLOCK_SIZE, dh), dtype=np.uint16)
+    packed_v = np.zeros((total, BLOCK_SIZE, dh), dtype=np.uint16)
+    kview, vview = pool.view("k"), pool.view("v")
+    for b in range(num_seqs):
+        for p in range(pages[b]):
+            c = int(offsets[b]) + p
+            compact[b, p] = c
+            blk = int(bt[b, p])
+            if 0 <= blk < pool.num_blocks:
+                packed_k[c] = kview[blk, :, kv_head, :]
+                packed_v[c] = vview[blk, :, kv_head, :]
+            else:
+                bad.add(b)
+                packed_k[c] = NAN_BITS
+                packed_v[c] = NAN_BITS
+    return Gathered(packed_k, packed_v, compact, offsets, sorted(bad), None)
+
+
+def pool_from_packed(packed_k: np.ndarray, packed_v: np.ndarray, capacity_pages: int) -> HostPool:
+    """A one-head HostPool ('separate' layout) whose first pages hold the
+    packed K/V bit patterns; pages past them keep the pool's NaN fill."""
+    total, bs, dh = packed_k.shape
+    pool = HostPool(max(capacity_pages, 1), 1, dh, "separate")
+    pool.view("k")[:total, :, 0, :] = packed_k
+    pool.view("v")[:total, :, 0, :] = packed_v
+    return pool

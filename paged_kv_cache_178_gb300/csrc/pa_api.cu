@@ -507,7 +507,69 @@ pa_status pa_check_errors(pa_stream_t stream, int64_t *first_bad_index)
         return PA_ERR_CUDA;
     if (first_bad_index)
         *first_bad_index = h.index;
+    if (h.code == kErrBudget)
+        return PA_ERR_WORKSPACE;
     return h.code == kErrTimeout ? PA_ERR_TIMEOUT : PA_ERR_BAD_METADATA;
+}
+
+pa_status pa_gather_kv_head(const pa_kv_cache *cache, int32_t kv_head, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                            void *packed_k, void *packed_v, int64_t capacity_pages, int32_t *compact_tables,
+                            int32_t *compact_offsets, pa_stream_t stream)
+{
+    pa_status st = check_cache(cache);
+    if (st != PA_OK)
+        return st;
+    if (kv_head < 0 || kv_head >= cache->num_kv_heads || num_seqs < 0 || max_blocks_per_seq <= 0 ||
+        capacity_pages < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs > kGatherMaxSeqsHost || (int64_t)num_seqs * max_blocks_per_seq > INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) {
+        snprintf(g_last_info, sizeof g_last_info, "gather_kv_head: empty batch (nothing launched)");
+        return PA_OK;
+    }
+    if (!block_tables || !seq_lens || !compact_tables || !compact_offsets)
+        return PA_ERR_INVALID_ARG;
+    if (capacity_pages > 0 && (!packed_k || !packed_v || !aligned16(packed_k) || !aligned16(packed_v)))
+        return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(compact_tables) | reinterpret_cast<uintptr_t>(compact_offsets) |
+         reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(seq_lens)) &
+        3u)
+        return PA_ERR_INVALID_ARG;
+    {
+        // the kernel writes its four outputs while it reads the pool and the
+        // metadata: no output may share a byte with an input or another output
+        const int64_t page_bytes = (int64_t)16 * cache->head_dim * 2;
+        const int64_t table_bytes = (int64_t)num_seqs * max_blocks_per_seq * 4;
+        const Span reads[4] = {span(cache->k, pool_view_bytes(cache)), span(cache->v, pool_view_bytes(cache)),
+                               span(block_tables, table_bytes), span(seq_lens, (int64_t)num_seqs * 4)};
+        const Span writes[4] = {span(packed_k, capacity_pages * page_bytes),
+                                span(packed_v, capacity_pages * page_bytes), span(compact_tables, table_bytes),
+                                span(compact_offsets, ((int64_t)num_seqs + 1) * 4)};
+        for (int i = 0; i < 4; ++i) {
+            for (const Span &r : reads)
+                if (overlaps(writes[i], r))
+                    return PA_ERR_INVALID_ARG;
+            for (int j = i + 1; j < 4; ++j)
+                if (overlaps(writes[i], writes[j]))
+                    return PA_ERR_INVALID_ARG;
+        }
+    }
+    ErrState *err = nullptr;
+    if ((st = device_setup(&err)) != PA_OK)
+        return st;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const cudaError_t e = launch_gather_kv_head(
+        cache->k, cache->v, cache->num_blocks, cache->block_stride, cache->token_stride, cache->head_stride,
+        kv_head, cache->head_dim, block_tables, max_blocks_per_seq, seq_lens, num_seqs, packed_k, packed_v,
+        capacity_pages, compact_tables, compact_offsets, err, reinterpret_cast<cudaStream_t>(stream), nsm);
+    snprintf(g_last_info, sizeof g_last_info, "gather_kv_head head=%d seqs=%d capacity_pages=%lld", kv_head,
+             num_seqs, (long long)capacity_pages);
+    return cuda_status(e);
 }
 
 }  // extern "C"

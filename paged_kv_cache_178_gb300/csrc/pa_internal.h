@@ -15,7 +15,7 @@ struct ErrState {
     long long index;
 };
 
-enum : unsigned int { kErrBadMetadata = 4u, kErrTimeout = 5u };
+enum : unsigned int { kErrBadMetadata = 4u, kErrTimeout = 5u, kErrBudget = 3u };
 
 __device__ __forceinline__ void record_error(ErrState *e, unsigned int code, long long index)
 {
@@ -82,6 +82,15 @@ cudaError_t init_attention_attributes();
 // Head dim 512: two-CTA clusters (pa_attn512.cu).
 cudaError_t init_attention512_attributes();
 cudaError_t launch_attention512(const AttnArgs &a, const AttnPlan &plan, ErrState *err, cudaStream_t stream);
+
+// Compact active-block gather of one KV head (pa_gather.cu).
+cudaError_t launch_gather_kv_head(const void *k, const void *v, int64_t num_blocks, int64_t block_stride,
+                                  int64_t token_stride, int64_t head_stride, int32_t kv_head, int32_t head_dim,
+                                  const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+                                  int32_t num_seqs, void *packed_k, void *packed_v, int64_t capacity_pages,
+                                  int32_t *compact_tables, int32_t *compact_offsets, ErrState *err,
+                                  cudaStream_t stream, int num_sms);
+constexpr int kGatherMaxSeqsHost = 512;
 
 // Encodes a tiled tensor map (driver entry point fetched at run time).
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,

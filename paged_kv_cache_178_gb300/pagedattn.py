@@ -37,7 +37,7 @@ PA_ERR_CUDA = 6
 
 EXPORTED = ("pa_init", "pa_reshape_and_cache", "pa_paged_attention_workspace_size",
             "pa_paged_attention", "pa_paged_attention_noalloc", "pa_reshape_and_paged_attention",
-            "pa_check_errors",
+            "pa_gather_kv_head", "pa_check_errors",
             "pa_status_string", "pa_last_launch_info")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -87,6 +87,9 @@ def load(path: str = LIB_PATH):
         lib.pa_reshape_and_paged_attention.argtypes = [
             vp, i64, vp, i64, i64, vp, vp, i64, i64, i32, ctypes.POINTER(PaKvCache), vp, i32, vp, vp, i32,
             i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+        lib.pa_gather_kv_head.restype = i32
+        lib.pa_gather_kv_head.argtypes = [ctypes.POINTER(PaKvCache), i32, vp, i32, vp, i32, vp, vp, i64, vp,
+                                          vp, vp]
         lib.pa_check_errors.restype = i32
         lib.pa_check_errors.argtypes = [vp, ctypes.POINTER(i64)]
         lib.pa_status_string.restype = ctypes.c_char_p
@@ -366,6 +369,46 @@ def prepare_reshape_and_paged_attention(key: torch.Tensor, value: torch.Tensor, 
                                    query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace,
                                    stream)
     return PreparedCall(load().pa_reshape_and_paged_attention, args, "pa_reshape_and_paged_attention", keep)
+
+
+def _validate_gather(k_cache: torch.Tensor, kv_head: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                     packed_k: torch.Tensor, packed_v: torch.Tensor, compact_tables: torch.Tensor,
+                     compact_offsets: torch.Tensor) -> int:
+    """Checks the gather inputs; returns the packed capacity in pages."""
+    num_seqs = seq_lens.numel()
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens), ("compact_tables", compact_tables),
+                    ("compact_offsets", compact_offsets)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or compact_tables.shape != block_tables.shape \
+            or compact_offsets.numel() != num_seqs + 1:
+        raise ValueError("metadata shapes disagree")
+    dh = k_cache.shape[3]
+    for t in (packed_k, packed_v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4 \
+                or tuple(t.shape[1:]) != (16, 1, dh):
+            raise ValueError("packed buffers must be contiguous BF16 CUDA tensors [capacity_pages, 16, 1, Dh]")
+    if packed_k.shape != packed_v.shape:
+        raise ValueError("packed K and V must have the same capacity")
+    if not 0 <= kv_head < k_cache.shape[2]:
+        raise ValueError("kv_head out of range")
+    return packed_k.shape[0]
+
+
+def gather_kv_head(k_cache: torch.Tensor, v_cache: torch.Tensor, kv_head: int, block_tables: torch.Tensor,
+                   seq_lens: torch.Tensor, packed_k: torch.Tensor, packed_v: torch.Tensor,
+                   compact_tables: torch.Tensor, compact_offsets: torch.Tensor,
+                   stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Pack the pages that block_tables/seq_lens select for one KV head into
+    packed_k/packed_v [capacity_pages, 16, 1, Dh] (a one-head pool of their
+    own), writing the compact table [B, max_blocks] and page offsets [B + 1]."""
+    c = cache_struct(k_cache, v_cache)
+    cap = _validate_gather(k_cache, kv_head, block_tables, seq_lens, packed_k, packed_v, compact_tables,
+                           compact_offsets)
+    _check(load().pa_gather_kv_head(ctypes.byref(c), kv_head, block_tables.data_ptr(), block_tables.shape[1],
+                                    seq_lens.data_ptr(), seq_lens.numel(), packed_k.data_ptr(),
+                                    packed_v.data_ptr(), cap, compact_tables.data_ptr(),
+                                    compact_offsets.data_ptr(), _stream_handle(stream)), "pa_gather_kv_head")
 
 
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:

@@ -165,3 +165,32 @@ def test_no_gpu_calls_report_cuda_error(lib):
 def test_launch_info_is_a_string(lib):
     s = pagedattn.last_launch_info()
     assert isinstance(s, str) and len(s) > 0
+
+
+def _gkv(lib, cache, head=0, bt=_BUF["bt"], maxblk=448, sl=_BUF["sl"], nseq=4, pk=_BUF["out"],
+         pv=_BUF["lse"], cap=1800, ct=_BUF["ws"], co=_BUF["qsl"]):
+    return lib.pa_gather_kv_head(ctypes.byref(cache), head, bt, maxblk, sl, nseq, pk, pv, cap, ct, co, None)
+
+
+def test_gather_validation_and_overlap(lib):
+    import torch
+    c = _cache()
+    assert _gkv(lib, c, head=2) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, head=-1) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, maxblk=0) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, cap=-1) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, nseq=513) == pagedattn.PA_ERR_UNSUPPORTED
+    assert _gkv(lib, c, nseq=512, maxblk=1 << 23) == pagedattn.PA_ERR_UNSUPPORTED  # table indices past int32
+    assert _gkv(lib, c, pk=_BUF["out"] + 8) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, co=_BUF["qsl"] + 2) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, ct=0) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, _cache(head_dim=64)) == pagedattn.PA_ERR_UNSUPPORTED
+    assert _gkv(lib, c, nseq=0) == pagedattn.PA_OK                        # nothing to launch
+    # outputs may not overlap the pool, the metadata or each other
+    assert _gkv(lib, c, pk=FAKE + 4096) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, ct=_BUF["bt"] + 64) == pagedattn.PA_ERR_INVALID_ARG
+    assert _gkv(lib, c, pv=_BUF["out"] + 1799 * 4096) == pagedattn.PA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert _gkv(lib, c) == pagedattn.PA_ERR_CUDA
+        assert _gkv(lib, c, pv=_BUF["out"] + 1800 * 4096) == pagedattn.PA_ERR_CUDA  # adjacent: fine
+        assert _gkv(lib, c, cap=0, pk=0, pv=0) == pagedattn.PA_ERR_CUDA  # offsets only
