@@ -411,6 +411,7 @@ def run_ours(args, ws, rank, local):
     }
     if not args.no_secondary:
         line["decode_scaled"] = measure_decode_scaled(args, dev, stream, ws, peaks, peak_src)
+        line["gather"] = measure_gather(args, dev, stream, ws, peaks, peak_src)
         line["prefill"] = measure_prefill(args, dev, stream, ws, peaks, peak_src)
         line["prefill_wide"] = measure_prefill(args, dev, stream, ws, peaks, peak_src, launches=20,
                                                wide=True)
@@ -491,6 +492,47 @@ def measure_decode_scaled(args, dev, stream, ws, peaks, peak_src, copies: int = 
             "gbs": round(gbs, 1), "us_per_launch": round(t * 1e6, 2), "bytes_per_launch": nbytes,
             "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
             "peak_source": f"{peak_src} hbm_gbs", "schedule": info}
+
+
+def measure_gather(args, dev, stream, ws, peaks, peak_src, copies: int = 16, launches: int = 50):
+    """Compact active-block gather of one KV head (pa_gather_kv_head) over the
+    decode length mix repeated `copies` times, alternating between the two KV
+    heads and two packed buffers.  Algorithmic bytes per launch: the selected
+    K and V pages of the head read once and written once, plus the table,
+    lengths, compact table and offsets."""
+    from paged_kv_cache_178_gb300 import pagedattn
+    from paged_kv_cache_178_gb300.device import DeviceWorkload
+    lens = list(wl.DECODE_LENS) * copies
+    total_pages = sum(wl.pages_needed(L) for L in lens)
+    w = wl.decode(seq_lens=lens, num_blocks=total_pages + 64)
+    dw = DeviceWorkload(w, device=str(dev), fill_bits=None)
+    dw.write_cache()
+    B, mb = w.block_table.shape
+    bufs = [(torch.empty((total_pages, 16, 1, 128), dtype=torch.bfloat16, device=dev),
+             torch.empty((total_pages, 16, 1, 128), dtype=torch.bfloat16, device=dev),
+             torch.empty((B, mb), dtype=torch.int32, device=dev),
+             torch.empty((B + 1,), dtype=torch.int32, device=dev)) for _ in range(2)]
+    calls = [pagedattn.prepare_gather_kv_head(dw.k_cache, dw.v_cache, h, dw.block_tables, dw.seq_lens,
+                                              *bufs[h], stream=stream) for h in range(2)]
+
+    def gather(i):
+        calls[i % 2]()
+
+    with torch.cuda.stream(stream):
+        gather(0)
+    torch.cuda.synchronize()
+    assert pagedattn.check_errors(stream) == (pagedattn.PA_OK, -1)
+    g = GraphedSteps(gather, 2, stream, chunk=50)
+    g.prepare(launches)
+    g.run(4)
+    t = time_graphed(g, launches, stream, ws) / launches
+    nbytes = 2 * 2 * total_pages * 16 * 128 * 2 + 2 * B * mb * 4 + B * 4 + (B + 1) * 4
+    gbs = nbytes / t / 1e9
+    return {"workload": f"gather of one KV head, B={B} (the decode length mix x{copies}), "
+                        f"{total_pages} pages of 16x128 BF16 each for K and V",
+            "gbs": round(gbs, 1), "us_per_launch": round(t * 1e6, 2), "bytes_per_launch": nbytes,
+            "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_source": f"{peak_src} hbm_gbs"}
 
 
 def _packed(tensors, device=None, pin=False):

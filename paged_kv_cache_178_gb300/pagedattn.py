@@ -411,6 +411,22 @@ def gather_kv_head(k_cache: torch.Tensor, v_cache: torch.Tensor, kv_head: int, b
                                     compact_offsets.data_ptr(), _stream_handle(stream)), "pa_gather_kv_head")
 
 
+def prepare_gather_kv_head(k_cache: torch.Tensor, v_cache: torch.Tensor, kv_head: int, block_tables: torch.Tensor,
+                           seq_lens: torch.Tensor, packed_k: torch.Tensor, packed_v: torch.Tensor,
+                           compact_tables: torch.Tensor, compact_offsets: torch.Tensor,
+                           stream: Optional[torch.cuda.Stream] = None) -> "PreparedCall":
+    """gather_kv_head validated and marshalled once; calling the result
+    re-issues the same C-ABI call (tensor contents may change, not storage)."""
+    c = cache_struct(k_cache, v_cache)
+    cap = _validate_gather(k_cache, kv_head, block_tables, seq_lens, packed_k, packed_v, compact_tables,
+                           compact_offsets)
+    keep = (c, k_cache, v_cache, block_tables, seq_lens, packed_k, packed_v, compact_tables, compact_offsets)
+    args = (ctypes.byref(c), kv_head, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+            seq_lens.numel(), packed_k.data_ptr(), packed_v.data_ptr(), cap, compact_tables.data_ptr(),
+            compact_offsets.data_ptr(), _stream_handle(stream))
+    return PreparedCall(load().pa_gather_kv_head, args, "pa_gather_kv_head", keep)
+
+
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
     """Synchronise the stream, read and clear the device error latch.
     Returns (status, first_bad_index)."""
