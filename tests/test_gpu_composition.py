@@ -135,3 +135,63 @@ def test_overlapping_output_is_rejected_before_launch():
                                               w.scale, dw.max_query_len, dw.max_seq_len,
                                               workspace=dw.workspace)
     assert e.value.status == pagedattn.PA_ERR_INVALID_ARG
+
+
+def _rewrite_case(seed=5):
+    """Decode workload with the whole cache written; new K/V for a mix of
+    positions: a first page, a middle page (key 1300: the first tile of the
+    sixth 256-key chunk), a last page, a block no table row holds, and a
+    padding slot (-1)."""
+    w = wl.decode()
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    torch.cuda.synchronize()
+    table = w.block_table
+    used = {int(x) for b, L in enumerate(w.seq_lens.tolist()) for x in table[b, :wl.pages_needed(L)].tolist()}
+    free = next(x for x in range(w.num_blocks) if x not in used)
+    slots = [int(table[1, 0]) * 16 + 0, int(table[0, 1300 // 16]) * 16 + 1300 % 16,
+             int(table[2, (4171 - 1) // 16]) * 16 + (4171 - 1) % 16, int(table[3, 0]) * 16 + 5,
+             free * 16 + 3, -1]
+    gen = torch.Generator().manual_seed(seed)
+    key = wl.bf16_randn((len(slots), 2, 128), gen).cuda()
+    value = wl.bf16_randn((len(slots), 2, 128), gen).cuda()
+    return w, dw, key, value, torch.tensor(slots, dtype=torch.int64, device="cuda")
+
+
+def test_rewrites_anywhere_in_the_tables_are_seen():
+    """With few new tokens the attention copies the pages they do not touch
+    before the write completes and waits only at the first tile holding one
+    of them.  New values in first, middle and last pages must all be seen:
+    the result equals the write followed by a separate attention call, and
+    differs from the attention over the old cache."""
+    w, dw, key, value, slots = _rewrite_case()
+    out_old, lse_old = dw.attention()
+    out, lse = dw.write_and_attend(key=key, value=value, slot_mapping=slots)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    w2, ref, key2, value2, slots2 = _rewrite_case()
+    pagedattn.reshape_and_cache(key2, value2, ref.k_cache, ref.v_cache, slots2)
+    out_r, lse_r = ref.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    _bits_equal(dw.pool, ref.pool, "rewrites: pool")
+    _bits_equal(out, out_r, "rewrites: out vs two calls")
+    _bits_equal(lse, lse_r, "rewrites: lse vs two calls")
+    changed = (lse.view(torch.int32) != lse_old.view(torch.int32)).any(dim=1).cpu().tolist()
+    print(f"requests whose lse moved: {changed}")
+    assert changed == [True, True, True, True]
+
+
+def test_write_outside_the_batch_leaves_attention_unchanged():
+    """New tokens only in a block no table row holds (and padding): no tile
+    of the attention waits for the write, the attention equals the one over
+    the old cache, and the write still lands."""
+    w, dw, key, value, slots = _rewrite_case()
+    out_old, lse_old = dw.attention()
+    sl = slots.clone()
+    sl[:4] = -1
+    out, lse = dw.write_and_attend(key=key, value=value, slot_mapping=sl)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    _bits_equal(out, out_old, "write outside the batch: out")
+    _bits_equal(lse, lse_old, "write outside the batch: lse")
+    free_slot = int(sl[4])
+    got = dw.k_cache[free_slot // 16, free_slot % 16]
+    _bits_equal(got, key[4], "write outside the batch: the written K row")
