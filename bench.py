@@ -322,6 +322,20 @@ def run_ours(args, ws, rank, local):
                                            "traffic": None, "peak_source": pf["peak_source"]}}),
                   flush=True)
         return
+    if args.workload == "gather":
+        ga = measure_gather(args, dev, stream, ws, peaks, peak_src, launches=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": ga["gbs"], "unit": "GB/s",
+                              "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
+                              "ms_per_step": ga["us_per_launch"] / 1e3, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                              "data": "synthetic", "config": {"workload": ga["workload"]},
+                              "gpu_launches": args.steps,
+                              "roofline": {"bound": "hbm", "achieved": ga["gbs"], "peak": ga["peak"],
+                                           "unit": "GB/s", "frac": ga["frac"], "traffic": None,
+                                           "peak_source": ga["peak_source"]}}),
+                  flush=True)
+        return
 
     w = wl.decode()
     R = args.replicas
@@ -356,6 +370,10 @@ def run_ours(args, ws, rank, local):
         r = i % R
         reps[r].attention(out=outs[r], lse=lses[r])
 
+    def attn_only_tile64(i):
+        r = i % R
+        reps[r].attention(out=outs[r], lse=lses[r], kv_tile=64)
+
     with torch.cuda.stream(stream):
         step(0)                                 # eager warm call (attributes, maps)
     torch.cuda.synchronize()
@@ -384,6 +402,10 @@ def run_ours(args, ws, rank, local):
     attn.run(max(args.warmup, 3))
     n_attn = max(args.steps, 200)
     t_attn = time_graphed(attn, n_attn, stream, ws) / n_attn
+    # The same launches in the second canon (64-key tiles).
+    attn64 = GraphedSteps(attn_only_tile64, R, stream)
+    attn64.run(max(args.warmup, 3))
+    t_attn64 = time_graphed(attn64, n_attn, stream, ws) / n_attn
     attn_bytes = attn_io_bytes(w)
     achieved = attn_bytes / t_attn / 1e9
 
@@ -408,11 +430,16 @@ def run_ours(args, ws, rank, local):
                      "bytes_per_launch": attn_bytes, "us_per_launch": round(t_attn * 1e6, 3),
                      "peak_source": f"{peak_src} hbm_gbs"},
         "clocks": clocks,
+        "decode_tile64": {"workload": "the same attention launches with 64-key KV tiles (second canon)",
+                          "gbs": round(attn_bytes / t_attn64 / 1e9, 1), "us_per_launch": round(t_attn64 * 1e6, 3),
+                          "frac": round(attn_bytes / t_attn64 / 1e9 / peaks["hbm_gbs"], 4),
+                          "peak_source": f"{peak_src} hbm_gbs"},
     }
     if not args.no_secondary:
         line["decode_scaled"] = measure_decode_scaled(args, dev, stream, ws, peaks, peak_src)
         line["gather"] = measure_gather(args, dev, stream, ws, peaks, peak_src)
         line["prefill"] = measure_prefill(args, dev, stream, ws, peaks, peak_src)
+        line["prefill_tile64"] = measure_prefill(args, dev, stream, ws, peaks, peak_src, kv_tile=64)
         line["prefill_wide"] = measure_prefill(args, dev, stream, ws, peaks, peak_src, launches=20,
                                                wide=True)
     if not args.no_e2e:
@@ -425,10 +452,12 @@ def run_ours(args, ws, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200, wide: bool = False):
+def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200, wide: bool = False,
+                    kv_tile: int = 0):
     """Causal prefill, attention launches alone over rotating replicas;
     TFLOP/s over causal algorithmic flops.  Default: B=1 Q=KV=4096 Dh=128;
-    wide: B=1 Q=KV=18432 Hq=16 Hkv=2 Dh=512."""
+    wide: B=1 Q=KV=18432 Hq=16 Hkv=2 Dh=512.  kv_tile: the fixed
+    arithmetic's KV tile (0: the head dim's default)."""
     from paged_kv_cache_178_gb300 import pagedattn
     from paged_kv_cache_178_gb300.device import DeviceWorkload
     w = wl.wide_head(args.wide_len) if wide else wl.long_prefill(4096)
@@ -439,7 +468,7 @@ def measure_prefill(args, dev, stream, ws, peaks, peak_src, launches: int = 200,
     lses = [torch.empty(dw.q.shape[:2], dtype=torch.float32, device=dev) for dw in reps]
 
     def attn(i):
-        reps[i % 4].attention(out=outs[i % 4], lse=lses[i % 4])
+        reps[i % 4].attention(out=outs[i % 4], lse=lses[i % 4], kv_tile=kv_tile)
 
     with torch.cuda.stream(stream):
         attn(0)
@@ -751,7 +780,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill", "wide"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "wide", "gather"], default="decode",
                     help="decode (default, the headline), or one causal prefill alone: "
                          "prefill (Dh=128, 4096) or wide (Dh=512, 18432)")
     ap.add_argument("--replicas", type=int, default=16)

@@ -77,6 +77,14 @@ typedef enum {
  * Offsets are computed in 64 bits, so a view may exceed 2**31 elements.
  * Requirements: block_size == 16; head_dim in {128, 256, 512}; k and v
  * 16-byte aligned; every stride a multiple of 8 elements (16 bytes).
+ * kv_tile selects the KV tile of the attention's fixed arithmetic ("fix(rocm):
+ * stabilize direct paged CK attention for bitwise R/R", Changes: fixed tile
+ * 128, tile 64 also supported; Additional checks: each tile passes the bitwise
+ * matrix on its own).  0 means 128 at head dims 128 and 256 and 64 at 512;
+ * head dim 128 also takes 64.  Results are bitwise reproducible within one
+ * tile (prefill, suffix and decode agree); the two tiles round differently.
+ * Another value returns PA_ERR_INVALID_ARG, a tile the head dim lacks
+ * PA_ERR_UNSUPPORTED.  The cache write and the gather ignore it.
  */
 typedef struct {
     void *k;
@@ -85,7 +93,7 @@ typedef struct {
     int32_t block_size;
     int32_t num_kv_heads;
     int32_t head_dim;
-    int32_t reserved; /* set to 0 */
+    int32_t kv_tile;  /* attention KV tile: 0 = the head dim's default (see below) */
     int64_t block_stride;
     int64_t token_stride;
     int64_t head_stride;

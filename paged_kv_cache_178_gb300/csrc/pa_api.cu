@@ -118,6 +118,19 @@ using namespace pa;
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The attention's KV tile: 0 (the head dim's default), or a tile that head
+// dim has -- 64 or 128 at head dim 128, 128 at 256, 64 at 512.
+static pa_status check_kv_tile(const pa_kv_cache *c)
+{
+    const int t = c->kv_tile;
+    if (t == 0)
+        return PA_OK;
+    if (t != 64 && t != 128)
+        return PA_ERR_INVALID_ARG;
+    const bool ok = c->head_dim == 128 || (c->head_dim == 256 && t == 128) || (c->head_dim == 512 && t == 64);
+    return ok ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 static pa_status check_cache(const pa_kv_cache *c)
 {
     if (!c || !c->k || !c->v)
@@ -236,6 +249,8 @@ static pa_status attention_check(const void *q, int64_t num_q_tokens, int64_t q_
     pa_status st = check_cache(cache);
     if (st != PA_OK)
         return st;
+    if ((st = check_kv_tile(cache)) != PA_OK)
+        return st;
     if (num_q_heads <= 0 || num_seqs < 0 || max_query_len < 0 || max_seq_len < 0 || num_q_tokens < 0 ||
         max_blocks_per_seq < 0)
         return PA_ERR_INVALID_ARG;
@@ -259,6 +274,8 @@ static pa_status attention_check(const void *q, int64_t num_q_tokens, int64_t q_
     if (!plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
                         pl))
         return PA_ERR_UNSUPPORTED;
+    if (cache->kv_tile != 0)
+        pl->kt = cache->kv_tile;
     if (pl->ws_bytes > 0) {
         if (!workspace || workspace_bytes < pl->ws_bytes)
             return PA_ERR_WORKSPACE;

@@ -86,18 +86,21 @@ constexpr int kSmallBytes = 512 /*barriers*/ + 64 /*flags*/ + 2 * 2 * kRows * 4 
 template <int DH>
 constexpr size_t tile_bytes() { return (size_t)(DH / 64) * 16384; }
 
-// One K stage: the 128-key tile, or with a CTA pair this CTA's 64 keys (all
-// of the head dim).  One V stage: the 128-key tile, or with a pair this CTA's
-// half of the head dim (all 128 keys).
-template <int DH, bool PAIR>
-constexpr size_t k_stage_bytes() { return PAIR ? tile_bytes<DH>() / 2 : tile_bytes<DH>(); }
-template <int DH, bool PAIR>
-constexpr size_t v_stage_bytes() { return PAIR ? tile_bytes<DH>() / 2 : tile_bytes<DH>(); }
+// One K stage: the KT-key tile, or with a CTA pair this CTA's KT/2 keys (all
+// of the head dim).  One V stage: the KT-key tile, or with a pair this CTA's
+// half of the head dim (all KT keys).
+template <int DH, bool PAIR, int KT>
+constexpr size_t k_stage_bytes() { return (size_t)(PAIR ? KT / 2 : KT) * DH * 2; }
+template <int DH, bool PAIR, int KT>
+constexpr size_t v_stage_bytes() { return (size_t)KT * (PAIR ? DH / 2 : DH) * 2; }
 
-template <int DH, bool PAIR>
-constexpr int stages_k() { return PAIR ? Cfg<DH>::kStagesKPair : Cfg<DH>::kStagesK; }
-template <int DH, bool PAIR>
-constexpr int stages_v() { return PAIR ? Cfg<DH>::kStagesVPair : Cfg<DH>::kStagesV; }
+// Stage counts are set for 128-key tiles; 64-key tiles take twice as many
+// stages of half the size, so the rings hold the same bytes (the split-KV
+// merge stages its operands in them).
+template <int DH, bool PAIR, int KT>
+constexpr int stages_k() { return (PAIR ? Cfg<DH>::kStagesKPair : Cfg<DH>::kStagesK) * (128 / KT); }
+template <int DH, bool PAIR, int KT>
+constexpr int stages_v() { return (PAIR ? Cfg<DH>::kStagesVPair : Cfg<DH>::kStagesV) * (128 / KT); }
 
 // CTA pairs with chunked heads keep two chunk accumulators in TMEM (columns
 // kOCol and kOCol + 128, by chunk parity) so the next chunk's P.V never waits
@@ -108,11 +111,11 @@ constexpr bool acc_in_smem() { return PAIR && Cfg<DH>::kChunk > 0; }
 template <int DH, bool PAIR>
 constexpr size_t acc_smem_bytes() { return acc_in_smem<DH, PAIR>() ? (size_t)kRows * DH * 4 : 0; }
 
-template <int DH, bool PAIR>
+template <int DH, bool PAIR, int KT>
 constexpr size_t smem_bytes()
 {
-    return 1024 /*alignment slack*/ + tile_bytes<DH>() /*Q*/ + k_stage_bytes<DH, PAIR>() * stages_k<DH, PAIR>() +
-           v_stage_bytes<DH, PAIR>() * stages_v<DH, PAIR>() + acc_smem_bytes<DH, PAIR>() + kSmallBytes;
+    return 1024 /*alignment slack*/ + tile_bytes<DH>() /*Q*/ + k_stage_bytes<DH, PAIR, KT>() * stages_k<DH, PAIR, KT>() +
+           v_stage_bytes<DH, PAIR, KT>() * stages_v<DH, PAIR, KT>() + acc_smem_bytes<DH, PAIR>() + kSmallBytes;
 }
 
 // Split-KV partial-state record of one chunk (fp32): m[R], l[R] padded to a
@@ -480,17 +483,24 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
 // The leader's thread issues all MMAs; tile-full barriers, P-ready and
 // fold-done barriers live in the leader, stage-release and S/PV-done commits
 // go to both CTAs.  Every row still sees the same operation sequence (C1-C6).
-template <int DH, bool PAIR>
+template <int DH, bool PAIR, int KT>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = Cfg<DH>;
+    constexpr int kKeys = KT;                        // keys per KV tile (the canon's tile: C1)
+    constexpr int PPT = kKeys / 16;                  // pages per KV tile
+    constexpr int TPL = 16 / PPT;                    // tiles whose block ids one 16-lane read covers
+    constexpr int HALF = kKeys / 2;                  // score columns per softmax half
+    constexpr int NPV = kKeys / 16;                  // K-steps of one P.V (16 keys each)
+    static_assert(KT == 128 || (KT == 64 && DH == 128), "KV tile");
     constexpr int NKB = DH / 64;                     // 64-column (128-byte) blocks of the head dim
     constexpr int TILE_BYTES = (int)tile_bytes<DH>();  // 128 rows x DH BF16 (the Q tile)
-    constexpr int NSK = stages_k<DH, PAIR>();
-    constexpr int NSV = stages_v<DH, PAIR>();
-    constexpr int KST = (int)k_stage_bytes<DH, PAIR>();
-    constexpr int VST = (int)v_stage_bytes<DH, PAIR>();
-    constexpr int KBLK = PAIR ? 8192 : 16384;        // bytes of one 64-column block of a K stage
+    constexpr int NSK = stages_k<DH, PAIR, KT>();
+    constexpr int NSV = stages_v<DH, PAIR, KT>();
+    constexpr int KST = (int)k_stage_bytes<DH, PAIR, KT>();
+    constexpr int VST = (int)v_stage_bytes<DH, PAIR, KT>();
+    constexpr int KBLK = (PAIR ? kKeys / 2 : kKeys) * 128;  // bytes of one 64-column block of a K stage
+    constexpr int VBLK = kKeys * 128;                // bytes of one 64-column block of a V stage
     constexpr int VKB = PAIR ? NKB / 2 : NKB;        // 64-column blocks of a V stage
     constexpr int CL = PAIR ? 2 : 1;
     constexpr bool CHUNKED = C::kChunk > 0;
@@ -547,6 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int warp = tid / 32, lane = tid % 32;
     float *const merge_work = reinterpret_cast<float *>(sK);
     constexpr int kMergeWorkFloats = (NSK * KST + NSV * VST) / 4;
+    // the split-KV merge's worst case (128 rows, one folder, one chunk per
+    // segment): running O, two (m, l) rows, then m/l, O, coefficients and
+    // mode of one chunk, with rounding slack.  Split-KV runs single CTAs.
+    static_assert(PAIR || !(C::kChunk > 0) || kMergeWorkFloats >= kRows * DH + 4 * kRows + kRows * (DH + 5) + 16,
+                  "split-KV merge staging does not fit the K/V stage area");
 
     // ---------------------------------------------------------- work unit --
     int b, kvh, qt, c_grid = 0;
@@ -610,10 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int64_t rec_floats = part_record_floats(p.ws_rows, DH);
     const int64_t rec_hdr = part_header_floats(p.ws_rows);
 
-    // The producer's first 16 block ids (two tiles) are requested before the
+    // The producer's first 16 block ids (TPL tiles) are requested before the
     // set-up barrier so the load overlaps it.
     auto load16 = [&](int t) {
-        const int pg = t * 8 + lane;
+        const int pg = t * PPT + lane;
         return (lane < 16 && pg < npages_need) ? __ldg(bt_row + pg) : 0;
     };
     int ids_cur = (warp == 0) ? load16(t_begin) : 0;
@@ -698,31 +713,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         if (p.early_reads)
             griddep_wait();  // the cache write has completed and is visible
-        // ids of tiles (2j, 2j+1) sit in lanes 0-15 of ids_cur; the next pair is
-        // requested one pair ahead
+        // ids of TPL consecutive tiles sit in lanes 0-15 of ids_cur; the next
+        // group is requested one group ahead
         int ids_next = 0;
         for (int it = 0; ok && it < n_it; ++it) {
             const int t = t_begin + it;
-            if ((it & 1) == 0) {
+            if (it % TPL == 0) {
                 if (it > 0)
                     ids_cur = ids_next;
-                if (it + 2 < n_it)
-                    ids_next = load16(t + 2);
+                if (it + TPL < n_it)
+                    ids_next = load16(t + TPL);
             }
-            int id = __shfl_sync(0xffffffffu, ids_cur, (it & 1) * 8 + (lane & 7));
-            const int np = min(8, npages_need - t * 8);
+            int id = __shfl_sync(0xffffffffu, ids_cur, (it % TPL) * PPT + (lane % PPT));
+            const int np = min(PPT, npages_need - t * PPT);
             const bool badl = lane < np && (id < 0 || (int64_t)id >= p.num_blocks);
             if (badl)
                 id = 0;  // keep the pipeline flowing; the rows become NaN
             any_bad |= __any_sync(0xffffffffu, badl);
             // K boxes: (page, 64-column block) per lane; a pair member takes the
             // pages of its 64 keys.  V boxes: all pages, this CTA's blocks.
-            const int k_page = (int)crank * 4 + lane / NKB, k_kb = lane % NKB;
-            const int k_id = __shfl_sync(0xffffffffu, id, k_page & 7);
-            const bool k_issue = lane < (8 / CL) * NKB && k_page < np;
+            const int k_page = (int)crank * (PPT / CL) + lane / NKB, k_kb = lane % NKB;
+            const int k_id = __shfl_sync(0xffffffffu, id, k_page % PPT);
+            const bool k_issue = lane < (PPT / CL) * NKB && k_page < np;
             const int v_page = lane / VKB, v_kb = lane % VKB;
-            const int v_id = __shfl_sync(0xffffffffu, id, v_page & 7);
-            const bool v_issue = lane < 8 * VKB && v_page < np;
+            const int v_id = __shfl_sync(0xffffffffu, id, v_page % PPT);
+            const bool v_issue = lane < PPT * VKB && v_page < np;
             // K
             const int sk = it % NSK, uk = it / NSK;
             if (lane == 0) {
@@ -735,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (!ok)
                 break;
             if (k_issue) {
-                const uint32_t dst = smem_addr(sK + sk * KST + k_kb * KBLK + (k_page - (int)crank * 4) * 2048);
+                const uint32_t dst = smem_addr(sK + sk * KST + k_kb * KBLK + (k_page - (int)crank * (PPT / CL)) * 2048);
                 if (PAIR)
                     tma_load_4d_pair(dst, &p.tm_k, lead_bar(B_KF + sk), k_kb * 64, kvh, 0, k_id);
                 else
@@ -764,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (!ok)
                 break;
             if (v_issue) {
-                const uint32_t dst = smem_addr(sV + sv * VST + v_kb * 16384 + v_page * 2048);
+                const uint32_t dst = smem_addr(sV + sv * VST + v_kb * VBLK + v_page * 2048);
                 const int col = ((int)crank * VKB + v_kb) * 64;
                 if (PAIR)
                     tma_load_4d_pair(dst, &p.tm_v, v_local ? bar(B_VF + sv) : lead_bar(B_VF + sv), col, kvh, 0,
@@ -791,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 for (int idx = lane; idx < nz; idx += 32) {
                     const int row = row0 + idx / (VKB * 8);
                     const int rem = idx % (VKB * 8);
-                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * 16384 + row * 128 + (rem % 8) * 16) =
+                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * VBLK + row * 128 + (rem % 8) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -833,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 for (int idx = lane; idx < nz; idx += 32) {
                     const int row = row0 + idx / (VKB * 8);
                     const int rem = idx % (VKB * 8);
-                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * 16384 + row * 128 + (rem % 8) * 16) =
+                    *reinterpret_cast<uint4 *>(vs + (rem / 8) * VBLK + row * 128 + (rem % 8) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -897,12 +912,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             // buffer, keys 64-127 in columns 64-95 (each softmax half writes
             // its own); V advances 16 keys (2048 bytes) per instruction
             const uint32_t pcol = tmem + (uint32_t)(j % NSB) * kKeys;
-            const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), 16384, 1024);
-            uint32_t ad[8];
-            uint64_t bd[8];
+            const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), VBLK, 1024);
+            uint32_t ad[NPV];
+            uint64_t bd[NPV];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                ad[i] = pcol + (uint32_t)((i / 4) * 64 + (i % 4) * 8);
+            for (int i = 0; i < NPV; ++i) {
+                ad[i] = pcol + (uint32_t)((i / (NPV / 2)) * HALF + (i % (NPV / 2)) * 8);
                 bd[i] = vd0 + (uint64_t)((i * 2048) >> 4);
             }
             const bool chunk_first = CHUNKED ? ((t * kKeys) % CHUNK_DIV == 0) : (j == 0);
@@ -924,7 +939,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             }
             if (okj) {
                 tc_fence_after();
-                mma8_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
+                if constexpr (NPV == 8)
+                    mma8_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
+                else
+                    mma4_ts<CL>(tmem + ocol(k), ad, bd, ID_PV, chunk_first ? 0u : 1u);
                 if (PAIR) {
                     mma_commit_pair_mc(bar(B_VE + sv), 0x3);
                     mma_commit_pair_mc(bar(B_PV + (j & 1)), 0x3);
@@ -991,16 +1009,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             bool okw = !failed && wb(B_SF + sb, (it / NSB) & 1);
             okw = __all_sync(0xffffffffu, okw);
             tc_fence_after();
-            const int nallow = row_valid ? max(0, min(64, pos - t * kKeys - 64 * h + 1)) : 0;
-            const uint32_t scol = tmem + lane_off + sb * kKeys + 64 * h;  // this half's S columns
+            const int nallow = row_valid ? max(0, min(HALF, pos - t * kKeys - HALF * h + 1)) : 0;
+            const uint32_t scol = tmem + lane_off + sb * kKeys + HALF * h;  // this half's S columns
             // pass 1: max of the raw scores over allowed keys of this half
             // (scale > 0, so this is the max of the scaled scores as well)
-            const bool unmasked = __all_sync(0xffffffffu, nallow == 64);
+            const bool unmasked = __all_sync(0xffffffffu, nallow == HALF);
             float pmax = -INFINITY;
             if (warp_active && okw) {
                 uint32_t v0[32], v1[32];
                 tmem_ld32(scol, v0);
-                tmem_ld32(scol + 32, v1);
+                if (HALF == 64)
+                    tmem_ld32(scol + 32, v1);
                 tmem_wait_ld();
                 if (unmasked) {
                     // two independent chains of three-input max (max is exact:
@@ -1008,15 +1027,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                     float pm0 = -INFINITY, pm1 = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        pm0 = max3f(pm0, __uint_as_float(v0[i]), __uint_as_float(v1[i]));
-                        pm1 = max3f(pm1, __uint_as_float(v0[i + 1]), __uint_as_float(v1[i + 1]));
+                        if (HALF == 64) {
+                            pm0 = max3f(pm0, __uint_as_float(v0[i]), __uint_as_float(v1[i]));
+                            pm1 = max3f(pm1, __uint_as_float(v0[i + 1]), __uint_as_float(v1[i + 1]));
+                        } else {
+                            pm0 = max3f(pm0, __uint_as_float(v0[i]), __uint_as_float(v0[i + 1]));
+                        }
                     }
                     pmax = fmaxf(pm0, pm1);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         pmax = (i < nallow) ? fmaxf(pmax, __uint_as_float(v0[i])) : pmax;
-                        pmax = (32 + i < nallow) ? fmaxf(pmax, __uint_as_float(v1[i])) : pmax;
+                        if (HALF == 64)
+                            pmax = (32 + i < nallow) ? fmaxf(pmax, __uint_as_float(v1[i])) : pmax;
                     }
                 }
             }
@@ -1046,10 +1070,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 // each lane is the scalar fma.rn / add.rn of the same operands
                 const uint64_t c2x2 = pack_f32x2(p.scale_log2, p.scale_log2);
                 const uint64_t nmx2 = pack_f32x2(-m_new, -m_new);
-                uint64_t a2[4];  // accumulator k sums columns k, k+8, ..., k+56 (pairs k, k+1)
-                uint32_t w[32];
+                uint64_t a2[4];  // accumulator k sums columns k, k+8, ..., k+HALF-8 (pairs k, k+1)
+                uint32_t w[HALF / 2];
 #pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2) {
+                for (int g2 = 0; g2 < HALF / 32; ++g2) {
                     uint32_t v[32];
                     tmem_ld32(scol + g2 * 32, v);
                     tmem_wait_ld();
@@ -1077,9 +1101,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                     unpack_f32x2(a2[k2], a[2 * k2], a[2 * k2 + 1]);
                 hs = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
                                __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
-                // P (BF16, two keys per column) overwrites this half's first 32 S
-                // columns, after both S loads above completed
-                tmem_st32(scol, w);
+                // P (BF16, two keys per column) overwrites this half's first
+                // HALF/2 S columns, after the S loads above completed
+                if constexpr (HALF == 64)
+                    tmem_st32(scol, w);
+                else
+                    tmem_st16(scol, w);
             }
             xsum[h * kRows + r] = hs;
             named_sync(1, 256);
@@ -1279,6 +1306,7 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
         return false;
     AttnPlan pl{};
     pl.head_dim = head_dim;
+    pl.kt = head_dim == 512 ? 64 : 128;  // the head dim's default tile
     pl.group = G;
     pl.tokens_per_tile = kRows / G;
     pl.qtiles = max_query_len > 0 ? (max_query_len + pl.tokens_per_tile - 1) / pl.tokens_per_tile : 0;
@@ -1314,17 +1342,19 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     return true;
 }
 
-template <int DH, bool PAIR>
+template <int DH, bool PAIR, int KT = 128>
 static cudaError_t set_smem_attribute()
 {
-    return cudaFuncSetAttribute(attn_kernel<DH, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_bytes<DH, PAIR>());
+    return cudaFuncSetAttribute(attn_kernel<DH, PAIR, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<DH, PAIR, KT>());
 }
 
 cudaError_t init_attention_attributes()
 {
     cudaError_t e;
     if ((e = set_smem_attribute<128, false>()) != cudaSuccess || (e = set_smem_attribute<128, true>()) != cudaSuccess ||
+        (e = set_smem_attribute<128, false, 64>()) != cudaSuccess ||
+        (e = set_smem_attribute<128, true, 64>()) != cudaSuccess ||
         (e = set_smem_attribute<256, false>()) != cudaSuccess || (e = set_smem_attribute<256, true>()) != cudaSuccess)
         return e;
     return init_attention512_attributes();
@@ -1404,7 +1434,9 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = pl.cl == 2 ? smem_bytes<DH, true>() : smem_bytes<DH, false>();
+    const bool kt64 = DH == 128 && pl.kt == 64;
+    cfg.dynamicSmemBytes = kt64 ? (pl.cl == 2 ? smem_bytes<DH, true, 64>() : smem_bytes<DH, false, 64>())
+                                : (pl.cl == 2 ? smem_bytes<DH, true, 128>() : smem_bytes<DH, false, 128>());
     cfg.stream = stream;
     // the kernel may be scheduled while the preceding kernel (typically the
     // cache write) still runs; it waits for it before its first global read
@@ -1417,9 +1449,14 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pl.cl == 2 ? 2 : 1;
+    if constexpr (DH == 128) {
+        if (kt64)
+            return pl.cl == 2 ? cudaLaunchKernelEx(&cfg, attn_kernel<DH, true, 64>, p)
+                              : cudaLaunchKernelEx(&cfg, attn_kernel<DH, false, 64>, p);
+    }
     if (pl.cl == 2)
-        return cudaLaunchKernelEx(&cfg, attn_kernel<DH, true>, p);
-    return cudaLaunchKernelEx(&cfg, attn_kernel<DH, false>, p);
+        return cudaLaunchKernelEx(&cfg, attn_kernel<DH, true, 128>, p);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<DH, false, 128>, p);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &pl, ErrState *err, cudaStream_t stream,
@@ -1430,7 +1467,7 @@ cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &pl, ErrState *er
                  pl.head_dim,
                  pl.split ? "split-kv" : (pl.head_dim == 512 ? "in-cta-pair" : (pl.cl == 2 ? "in-cta-pair2sm" : "in-cta")),
                  pl.grid,
-                 pl.qtiles, pl.nch, pl.head_dim == 512 ? 64 : kKeys, pl.head_dim == 128 ? Cfg<128>::kChunk : 0,
+                 pl.qtiles, pl.nch, pl.kt, pl.head_dim == 128 ? Cfg<128>::kChunk : 0,
                  pl.cpu);
     if (pl.grid == 0)
         return cudaSuccess;

@@ -27,7 +27,7 @@ constexpr int kGatherThreads = 512;
 constexpr int kGatherMaxSeqs = kGatherThreads;  // one request per thread in the scan
 constexpr int kGatherPagesPerPass = 4;          // pages in flight per CTA pass
 
-__global__ void __launch_bounds__(kGatherThreads) gather_kv_head_kernel(
+__global__ void __launch_bounds__(kGatherThreads, 3) gather_kv_head_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, int64_t num_blocks, int64_t block_stride,
     int64_t token_stride, int64_t head_off, int32_t vecs_per_row, const int32_t *__restrict__ block_tables,
     int32_t max_blocks, const int32_t *__restrict__ seq_lens, int32_t num_seqs, uint4 *__restrict__ packed_k,
@@ -89,36 +89,50 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kv_head_kernel(
         compact_tables[e] = p < nb ? s_off[b] + p : -1;
     }
     // pages: kGatherPagesPerPass per CTA pass, every vector loaded before any
-    // is stored
+    // is stored; the block ids of the next pass are read while this pass's
+    // vectors are in flight
     const int vecs_page = 16 * vecs_per_row;  // 16-byte vectors of one K (or V) page
     const uint4 qnan = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-    for (int64_t c0 = (int64_t)blockIdx.x * kGatherPagesPerPass; c0 < total;
-         c0 += (int64_t)gridDim.x * kGatherPagesPerPass) {
+    // block id of packed page c (raw, unchecked), and its request
+    auto page_id = [&](int64_t c, int &req) -> int {
+        // request of packed page c: the last b with s_off[b] <= c
+        int lo = 0, hi = num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_off[mid] <= c)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        req = lo;
+        return __ldg(block_tables + (int64_t)lo * max_blocks + (c - s_off[lo]));
+    };
+    const int64_t stride = (int64_t)gridDim.x * kGatherPagesPerPass;
+    int next_id[kGatherPagesPerPass], next_req[kGatherPagesPerPass];
+    int64_t c0 = (int64_t)blockIdx.x * kGatherPagesPerPass;
+#pragma unroll
+    for (int j = 0; j < kGatherPagesPerPass; ++j)
+        next_id[j] = (c0 + j < total) ? page_id(c0 + j, next_req[j]) : 0;
+    for (; c0 < total; c0 += stride) {
         int64_t src_page[kGatherPagesPerPass];
 #pragma unroll
         for (int j = 0; j < kGatherPagesPerPass; ++j) {
-            const int64_t c = c0 + j;
             src_page[j] = -2;  // past the last page: nothing to do
-            if (c < total) {
-                // request of packed page c: the last b with s_off[b] <= c
-                int lo = 0, hi = num_seqs - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (s_off[mid] <= c)
-                        lo = mid;
-                    else
-                        hi = mid - 1;
-                }
-                const int id = __ldg(block_tables + (int64_t)lo * max_blocks + (c - s_off[lo]));
+            if (c0 + j < total) {
+                const int id = next_id[j];
                 if (id < 0 || (int64_t)id >= num_blocks) {
                     if (tid == 0)
-                        record_error(err, kErrBadMetadata, lo);
+                        record_error(err, kErrBadMetadata, next_req[j]);
                     src_page[j] = -1;  // NaN page
                 } else {
                     src_page[j] = id;
                 }
             }
         }
+        const int64_t c1 = c0 + stride;
+#pragma unroll
+        for (int j = 0; j < kGatherPagesPerPass; ++j)
+            next_id[j] = (c1 + j < total) ? page_id(c1 + j, next_req[j]) : 0;
         for (int e = tid; e < 2 * vecs_page; e += blockDim.x) {
             const int which = e / vecs_page, r = e % vecs_page;
             const int t = r / vecs_per_row, d = r % vecs_per_row;
@@ -145,10 +159,16 @@ cudaError_t launch_gather_kv_head(const void *k, const void *v, int64_t num_bloc
                                   int32_t *compact_tables, int32_t *compact_offsets, ErrState *err,
                                   cudaStream_t stream, int num_sms)
 {
-    // pages of the largest batch the bounds allow, a few CTAs per SM at most
+    // pages of the largest batch the bounds allow, at most one wave of
+    // resident CTAs (no tail wave)
     const int64_t max_pages = (int64_t)num_seqs * max_blocks;
     int64_t grid = (max_pages + kGatherPagesPerPass - 1) / kGatherPagesPerPass;
-    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * 4;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kv_head_kernel, kGatherThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * per_sm;
     if (grid > cap)
         grid = cap;
     if (grid < 1)

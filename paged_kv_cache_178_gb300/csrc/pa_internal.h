@@ -67,6 +67,7 @@ struct AttnPlan {
     size_t ws_counter_bytes;
     size_t ws_bytes;    // total workspace needed
     long long grid;     // CTAs (or clusters x 2 for Dh=512)
+    int kt;             // keys per KV tile: the fixed arithmetic's tile (64 or 128)
 };
 
 bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

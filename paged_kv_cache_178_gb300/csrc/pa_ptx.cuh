@@ -321,6 +321,30 @@ __device__ __forceinline__ void mma8_ts(uint32_t d_tmem, const uint32_t (&a)[8],
                      : "memory");
 }
 
+// Four A-from-tensor-memory MMAs (K = 64), the same way.
+#define PA_MMA4_BODY(CG)                                                                                 \
+    "{\n\t.reg .pred p0, p1;\n\t"                                                                         \
+    "setp.ne.b32 p0, %10, 0;\n\t"                                                                         \
+    "setp.ne.b32 p1, 1, 0;\n\t"                                                                           \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], [%1], %5, %9, p0;\n\t"                                \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], [%2], %6, %9, p1;\n\t"                                \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], [%3], %7, %9, p1;\n\t"                                \
+    "tcgen05.mma.cta_group::" #CG ".kind::f16 [%0], [%4], %8, %9, p1;\n\t}"
+
+template <int CG>
+__device__ __forceinline__ void mma4_ts(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                        uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (CG == 1)
+        asm volatile(PA_MMA4_BODY(1)::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]),
+                     "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile(PA_MMA4_BODY(2)::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]),
+                     "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(accumulate)
+                     : "memory");
+}
+
 // ------------------------------------------------- CTA pairs (cta_group::2) --
 // A kernel uses one cta_group value for all of its tcgen05 instructions; the
 // pair variants below serve kernels where an even/odd CTA pair of a cluster

@@ -55,7 +55,7 @@ class DeviceWorkload:
 
     def attention(self, out=None, lse=None, want_lse=True, max_query_len=None, max_seq_len=None,
                   block_tables=None, q=None, seq_lens=None, query_start_loc=None, workspace=None,
-                  stream=None):
+                  stream=None, kv_tile=0):
         mq = self.max_query_len if max_query_len is None else max_query_len
         ms = self.max_seq_len if max_seq_len is None else max_seq_len
         if workspace is not None:
@@ -69,17 +69,19 @@ class DeviceWorkload:
             self.block_tables if block_tables is None else block_tables,
             self.seq_lens if seq_lens is None else seq_lens,
             self.query_start_loc if query_start_loc is None else query_start_loc,
-            self.w.scale, mq, ms, out=out, lse=lse, want_lse=want_lse, workspace=ws, stream=stream)
+            self.w.scale, mq, ms, out=out, lse=lse, want_lse=want_lse, workspace=ws, stream=stream,
+            kv_tile=kv_tile)
 
     def write_and_attend(self, key=None, value=None, slot_mapping=None, out=None, lse=None, want_lse=True,
-                         stream=None):
+                         stream=None, kv_tile=0):
         """The cache write of (key, value, slot_mapping) -- by default every
         token of the workload -- and the attention, in one library call."""
         return pagedattn.reshape_and_paged_attention(
             self.key if key is None else key, self.value if value is None else value,
             self.slot_mapping if slot_mapping is None else slot_mapping, self.q, self.k_cache, self.v_cache,
             self.block_tables, self.seq_lens, self.query_start_loc, self.w.scale, self.max_query_len,
-            self.max_seq_len, out=out, lse=lse, want_lse=want_lse, workspace=self.workspace, stream=stream)
+            self.max_seq_len, out=out, lse=lse, want_lse=want_lse, workspace=self.workspace, stream=stream,
+            kv_tile=kv_tile)
 
     def share_cache_with(self, other: "DeviceWorkload") -> None:
         """Point this workload at another's pool (same geometry)."""

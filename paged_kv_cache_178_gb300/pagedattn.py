@@ -45,7 +45,7 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 class PaKvCache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
                 ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_tile", ctypes.c_int32),
                 ("block_stride", ctypes.c_int64), ("token_stride", ctypes.c_int64),
                 ("head_stride", ctypes.c_int64)]
 
@@ -124,8 +124,9 @@ def last_launch_info() -> str:
     return buf.value.decode()
 
 
-def cache_struct(k_cache: torch.Tensor, v_cache: torch.Tensor) -> PaKvCache:
-    """Describe a [num_blocks, 16, Hkv, Dh] K/V pair for the C ABI."""
+def cache_struct(k_cache: torch.Tensor, v_cache: torch.Tensor, kv_tile: int = 0) -> PaKvCache:
+    """Describe a [num_blocks, 16, Hkv, Dh] K/V pair for the C ABI.  kv_tile:
+    the attention's KV tile (0: the head dim's default; 64 or 128 at Dh=128)."""
     for t in (k_cache, v_cache):
         if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4:
             raise ValueError("caches must be 4-D BF16 CUDA tensors [num_blocks, 16, Hkv, Dh]")
@@ -134,7 +135,7 @@ def cache_struct(k_cache: torch.Tensor, v_cache: torch.Tensor) -> PaKvCache:
     if k_cache.shape != v_cache.shape or k_cache.stride() != v_cache.stride():
         raise ValueError("K and V caches must have the same shape and strides")
     nb, bs, hkv, dh = k_cache.shape
-    return PaKvCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, dh, 0, k_cache.stride(0),
+    return PaKvCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, dh, int(kv_tile), k_cache.stride(0),
                      k_cache.stride(1), k_cache.stride(2))
 
 
@@ -201,11 +202,12 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                     max_seq_len: int, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, want_lse: bool = True,
                     workspace: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None
+                    stream: Optional[torch.cuda.Stream] = None, kv_tile: int = 0
                     ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Causal GQA attention of q [Tq, Hq, Dh] over the paged caches.
-    Returns (out [Tq, Hq, Dh] BF16, lse [Tq, Hq] fp32 or None)."""
-    c = cache_struct(k_cache, v_cache)
+    Returns (out [Tq, Hq, Dh] BF16, lse [Tq, Hq] fp32 or None).  kv_tile
+    selects the fixed arithmetic's KV tile (see cache_struct)."""
+    c = cache_struct(k_cache, v_cache, kv_tile)
     tq, hq, dh, num_seqs = _validate_attention(q, block_tables, seq_lens, query_start_loc)
     if out is None:
         out = torch.empty((tq, hq, dh), dtype=torch.bfloat16, device=q.device)
@@ -233,13 +235,13 @@ def paged_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             block_tables: torch.Tensor, seq_lens: torch.Tensor,
                             query_start_loc: torch.Tensor, scale: float, max_query_len: int,
                             max_seq_len: int, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
-                            stream: Optional[torch.cuda.Stream] = None) -> int:
+                            stream: Optional[torch.cuda.Stream] = None, kv_tile: int = 0) -> int:
     """paged_attention for callers that cannot allocate: no workspace and no
     output allocation here (out, and lse if wanted, are passed in); the
     library's built-in scratch array is used instead.  Returns the status
     code (PA_ERR_WORKSPACE when the bounds need more than
     NOALLOC_SCRATCH_BYTES) rather than raising."""
-    c = cache_struct(k_cache, v_cache)
+    c = cache_struct(k_cache, v_cache, kv_tile)
     tq, hq, dh = q.shape
     return int(load().pa_paged_attention_noalloc(
         q.data_ptr(), tq, q.stride(0), hq, ctypes.byref(c), block_tables.data_ptr(),
@@ -281,10 +283,10 @@ def prepare_paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             query_start_loc: torch.Tensor, scale: float, max_query_len: int,
                             max_seq_len: int, out: torch.Tensor, lse: Optional[torch.Tensor],
                             workspace: Optional[torch.Tensor],
-                            stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+                            stream: Optional[torch.cuda.Stream] = None, kv_tile: int = 0) -> PreparedCall:
     """paged_attention into given out / lse / workspace, validated now and
     issued by each call of the result."""
-    c = cache_struct(k_cache, v_cache)
+    c = cache_struct(k_cache, v_cache, kv_tile)
     tq, hq, dh, num_seqs = _validate_attention(q, block_tables, seq_lens, query_start_loc)
     if out.shape != (tq, hq, dh) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [Tq, Hq, Dh] BF16 tensor")
@@ -305,8 +307,8 @@ def prepare_paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
 
 
 def _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens,
-                      query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace, stream):
-    c = cache_struct(k_cache, v_cache)
+                      query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace, stream, kv_tile):
+    c = cache_struct(k_cache, v_cache, kv_tile)
     n = _validate_write(key, value, slot_mapping)
     tq, hq, dh, num_seqs = _validate_attention(q, block_tables, seq_lens, query_start_loc)
     if out.shape != (tq, hq, dh) or out.dtype != torch.bfloat16 or not out.is_contiguous():
@@ -335,7 +337,7 @@ def reshape_and_paged_attention(key: torch.Tensor, value: torch.Tensor, slot_map
                                 max_seq_len: int, out: Optional[torch.Tensor] = None,
                                 lse: Optional[torch.Tensor] = None, want_lse: bool = True,
                                 workspace: Optional[torch.Tensor] = None,
-                                stream: Optional[torch.cuda.Stream] = None
+                                stream: Optional[torch.cuda.Stream] = None, kv_tile: int = 0
                                 ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """reshape_and_cache of key/value at slot_mapping, then paged_attention of q
     over the updated caches, in one library call whose attention grid starts
@@ -351,7 +353,7 @@ def reshape_and_paged_attention(key: torch.Tensor, value: torch.Tensor, slot_map
             workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     args, _keep = _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens,
                                     query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace,
-                                    stream)
+                                    stream, kv_tile)
     _check(load().pa_reshape_and_paged_attention(*args), "pa_reshape_and_paged_attention")
     return out, lse
 
@@ -362,12 +364,13 @@ def prepare_reshape_and_paged_attention(key: torch.Tensor, value: torch.Tensor, 
                                         query_start_loc: torch.Tensor, scale: float, max_query_len: int,
                                         max_seq_len: int, out: torch.Tensor, lse: Optional[torch.Tensor],
                                         workspace: Optional[torch.Tensor],
-                                        stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+                                        stream: Optional[torch.cuda.Stream] = None,
+                                        kv_tile: int = 0) -> PreparedCall:
     """reshape_and_paged_attention into given out / lse / workspace, validated
     now and issued by each call of the result."""
     args, keep = _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_tables, seq_lens,
                                    query_start_loc, scale, max_query_len, max_seq_len, out, lse, workspace,
-                                   stream)
+                                   stream, kv_tile)
     return PreparedCall(load().pa_reshape_and_paged_attention, args, "pa_reshape_and_paged_attention", keep)
 
 

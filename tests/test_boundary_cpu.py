@@ -49,7 +49,7 @@ FAKE = 0x10000000  # aligned, never dereferenced: validation fails before any CU
 
 def _cache(**kw):
     c = dict(k=FAKE, v=FAKE + 0x1000, num_blocks=2048, block_size=16, num_kv_heads=2, head_dim=128,
-             reserved=0, block_stride=2 * 16 * 2 * 128, token_stride=2 * 128, head_stride=128)
+             kv_tile=0, block_stride=2 * 16 * 2 * 128, token_stride=2 * 128, head_stride=128)
     c.update(kw)
     return pagedattn.PaKvCache(**c)
 
@@ -96,6 +96,15 @@ def test_attention_validation(lib):
     assert _attn(lib, c, ws=FAKE + 16, ws_len=ws) == pagedattn.PA_ERR_INVALID_ARG
     assert _attn(lib, c, nseq=0) == pagedattn.PA_OK                        # empty batch
     assert _attn(lib, c, mq=-1) == pagedattn.PA_ERR_INVALID_ARG
+    # the attention's KV tile: 0 or a tile the head dim has
+    assert _attn(lib, _cache(kv_tile=32)) == pagedattn.PA_ERR_INVALID_ARG
+    assert _attn(lib, _cache(kv_tile=64), nseq=0) == pagedattn.PA_OK
+    assert _attn(lib, _cache(kv_tile=128), nseq=0) == pagedattn.PA_OK
+    dh256 = dict(head_dim=256, head_stride=256, token_stride=512, block_stride=2 * 16 * 512)
+    assert _attn(lib, _cache(kv_tile=64, **dh256)) == pagedattn.PA_ERR_UNSUPPORTED
+    dh512 = dict(head_dim=512, head_stride=512, token_stride=1024, block_stride=2 * 16 * 1024)
+    assert _attn(lib, _cache(kv_tile=128, **dh512)) == pagedattn.PA_ERR_UNSUPPORTED
+    assert _rc(lib, _cache(kv_tile=32), n=0) == pagedattn.PA_OK           # the cache write ignores it
 
 
 # Buffers for the one-call composition, 16 MB apart and clear of the fake
