@@ -52,7 +52,6 @@
 
 namespace pa {
 
-constexpr int kKeys = 128;          // keys per KV tile
 constexpr int kThreads = 512;
 constexpr int kSplitCtaThreshold = 152;
 

@@ -27,9 +27,12 @@ constexpr int kGatherThreads = 512;
 constexpr int kGatherMaxSeqs = kGatherThreads;  // one request per thread in the scan
 constexpr int kGatherPagesPerPass = 4;          // pages in flight per CTA pass
 
+// VPR: 16-byte vectors per K (or V) row of one head (head dim / 8), so the
+// index arithmetic below is shifts and masks.
+template <int VPR>
 __global__ void __launch_bounds__(kGatherThreads, 3) gather_kv_head_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, int64_t num_blocks, int64_t block_stride,
-    int64_t token_stride, int64_t head_off, int32_t vecs_per_row, const int32_t *__restrict__ block_tables,
+    int64_t token_stride, int64_t head_off, const int32_t *__restrict__ block_tables,
     int32_t max_blocks, const int32_t *__restrict__ seq_lens, int32_t num_seqs, uint4 *__restrict__ packed_k,
     uint4 *__restrict__ packed_v, int64_t capacity_pages, int32_t *__restrict__ compact_tables,
     int32_t *__restrict__ compact_offsets, ErrState *err)
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(kGatherThreads, 3) gather_kv_head_kernel(
     // pages: kGatherPagesPerPass per CTA pass, every vector loaded before any
     // is stored; the block ids of the next pass are read while this pass's
     // vectors are in flight
-    const int vecs_page = 16 * vecs_per_row;  // 16-byte vectors of one K (or V) page
+    constexpr int vecs_page = 16 * VPR;  // 16-byte vectors of one K (or V) page
     const uint4 qnan = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
     // block id of packed page c (raw, unchecked), and its request
     auto page_id = [&](int64_t c, int &req) -> int {
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kGatherThreads, 3) gather_kv_head_kernel(
             next_id[j] = (c1 + j < total) ? page_id(c1 + j, next_req[j]) : 0;
         for (int e = tid; e < 2 * vecs_page; e += blockDim.x) {
             const int which = e / vecs_page, r = e % vecs_page;
-            const int t = r / vecs_per_row, d = r % vecs_per_row;
+            const int t = r / VPR, d = r % VPR;
             const uint4 *src = which ? v : k;
             uint4 *dst = which ? packed_v : packed_k;
             uint4 val[kGatherPagesPerPass];
@@ -163,9 +166,12 @@ cudaError_t launch_gather_kv_head(const void *k, const void *v, int64_t num_bloc
     // resident CTAs (no tail wave)
     const int64_t max_pages = (int64_t)num_seqs * max_blocks;
     int64_t grid = (max_pages + kGatherPagesPerPass - 1) / kGatherPagesPerPass;
+    void (*kern)(const uint4 *, const uint4 *, int64_t, int64_t, int64_t, int64_t, const int32_t *, int32_t,
+                 const int32_t *, int32_t, uint4 *, uint4 *, int64_t, int32_t *, int32_t *, ErrState *) =
+        head_dim == 128 ? gather_kv_head_kernel<16>
+                        : (head_dim == 256 ? gather_kv_head_kernel<32> : gather_kv_head_kernel<64>);
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kv_head_kernel, kGatherThreads, 0) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGatherThreads, 0) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * per_sm;
@@ -182,9 +188,9 @@ cudaError_t launch_gather_kv_head(const void *k, const void *v, int64_t num_bloc
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gather_kv_head_kernel, static_cast<const uint4 *>(k),
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint4 *>(k),
                               static_cast<const uint4 *>(v), num_blocks, block_stride / 8, token_stride / 8,
-                              (int64_t)kv_head * head_stride / 8, (int32_t)(head_dim / 8), block_tables,
+                              (int64_t)kv_head * head_stride / 8, block_tables,
                               max_blocks, seq_lens, num_seqs, static_cast<uint4 *>(packed_k),
                               static_cast<uint4 *>(packed_v), capacity_pages, compact_tables, compact_offsets,
                               err);
