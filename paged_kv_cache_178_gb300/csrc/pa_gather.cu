@@ -110,22 +110,23 @@ __global__ void __launch_bounds__(kGatherThreads, 3) gather_kv_head_kernel(
         req = lo;
         return __ldg(block_tables + (int64_t)lo * max_blocks + (c - s_off[lo]));
     };
+    // lane j of every warp looks up page j of a pass; the others read it with
+    // a shuffle
     const int64_t stride = (int64_t)gridDim.x * kGatherPagesPerPass;
-    int next_id[kGatherPagesPerPass], next_req[kGatherPagesPerPass];
     int64_t c0 = (int64_t)blockIdx.x * kGatherPagesPerPass;
-#pragma unroll
-    for (int j = 0; j < kGatherPagesPerPass; ++j)
-        next_id[j] = (c0 + j < total) ? page_id(c0 + j, next_req[j]) : 0;
+    int next_id = 0, next_req = 0;
+    if (lane < kGatherPagesPerPass && c0 + lane < total)
+        next_id = page_id(c0 + lane, next_req);
     for (; c0 < total; c0 += stride) {
         int64_t src_page[kGatherPagesPerPass];
 #pragma unroll
         for (int j = 0; j < kGatherPagesPerPass; ++j) {
+            const int id = __shfl_sync(0xffffffffu, next_id, j);
             src_page[j] = -2;  // past the last page: nothing to do
             if (c0 + j < total) {
-                const int id = next_id[j];
                 if (id < 0 || (int64_t)id >= num_blocks) {
-                    if (tid == 0)
-                        record_error(err, kErrBadMetadata, next_req[j]);
+                    if (tid == j)
+                        record_error(err, kErrBadMetadata, next_req);
                     src_page[j] = -1;  // NaN page
                 } else {
                     src_page[j] = id;
@@ -133,9 +134,8 @@ __global__ void __launch_bounds__(kGatherThreads, 3) gather_kv_head_kernel(
             }
         }
         const int64_t c1 = c0 + stride;
-#pragma unroll
-        for (int j = 0; j < kGatherPagesPerPass; ++j)
-            next_id[j] = (c1 + j < total) ? page_id(c1 + j, next_req[j]) : 0;
+        if (lane < kGatherPagesPerPass && c1 + lane < total)
+            next_id = page_id(c1 + lane, next_req);
         for (int e = tid; e < 2 * vecs_page; e += blockDim.x) {
             const int which = e / vecs_page, r = e % vecs_page;
             const int t = r / VPR, d = r % VPR;
