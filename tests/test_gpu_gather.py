@@ -165,3 +165,43 @@ def test_bad_block_id_and_bad_length():
     n = int(g.offsets[-1])
     assert np.array_equal(co.cpu().numpy(), g.offsets) and np.array_equal(ct.cpu().numpy(), g.compact_tables)
     assert np.array_equal(_u16(pk[:n, :, 0]), g.packed_k) and (_u16(pk[n:]) == FILL).all()
+
+
+def test_prepared_gather_in_a_graph_repeats_eager():
+    """The prepared call captured in a CUDA graph and replayed gives the
+    eager call's bytes (metadata, packed pages), head after head."""
+    w = wl.decode(reversed_pages=True)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    total = sum(wl.pages_needed(int(L)) for L in w.seq_lens)
+    dev = dw.q.device
+    ref = []
+    for h in range(2):
+        pk, pv, ct, co = _buffers(dev, total, 128, 4, w.block_table.shape[1])
+        pagedattn.gather_kv_head(dw.k_cache, dw.v_cache, h, dw.block_tables, dw.seq_lens, pk, pv, ct, co)
+        ref.append((pk, pv, ct, co))
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    s = torch.cuda.Stream()
+    bufs = [_buffers(dev, total, 128, 4, w.block_table.shape[1]) for _ in range(2)]
+    calls = [pagedattn.prepare_gather_kv_head(dw.k_cache, dw.v_cache, h, dw.block_tables, dw.seq_lens, *bufs[h],
+                                              stream=s) for h in range(2)]
+    pagedattn.init()
+    with torch.cuda.stream(s):
+        calls[0]()
+    s.synchronize()
+    for b in bufs:
+        for t in b:
+            t.fill_(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls[0]()
+        calls[1]()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    for h in range(2):
+        for a, b, what in zip(bufs[h], ref[h], ("packed K", "packed V", "compact table", "offsets")):
+            same = torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+            print(f"graph replay head {h}: {what} equal={same}")
+            assert same

@@ -50,3 +50,23 @@ def test_noalloc_rejects_bounds_beyond_its_scratch():
                                            dw.query_start_loc, w.scale, 1, big, out)
     assert st == pagedattn.PA_ERR_WORKSPACE
     assert int(out.abs().sum()) == 0   # nothing was launched
+
+
+def test_noalloc_in_the_64_key_canon_equals_regular():
+    """The tile rides in the pool descriptor, so the allocation-free entry
+    point runs the same canon: bit for bit the regular call's results."""
+    w = wl.decode()
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    ref_out, ref_lse = dw.attention(kv_tile=64)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    st = pagedattn.paged_attention_noalloc(dw.q, dw.k_cache, dw.v_cache, dw.block_tables, dw.seq_lens,
+                                           dw.query_start_loc, w.scale, w.max_query_len, w.max_seq_len, out, lse,
+                                           kv_tile=64)
+    assert st == pagedattn.PA_OK, pagedattn.status_string(st)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    assert "kv_tile=64" in pagedattn.last_launch_info()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
