@@ -277,15 +277,32 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
         //     a chunk without keys holds -inf), so each (row, chunk) can be
         //     computed on its own; fold_coef's mixing factors depend only on
         //     that max and the chunk's own.
-        for (int i = tid; i < cn * rv; i += nth) {
-            const int c = i / rv, r = i % rv;
-            float mprev = s_run[2 * r];
-            for (int c2 = 0; c2 < c; ++c2)
-                mprev = fmaxf(mprev, s_ml[(c2 * rv + r) * 2]);
-            const Fold f = fold_coef(mprev, 0.f, s_ml[(c * rv + r) * 2], 0.f);
-            s_cf[(c * rv + r) * 2] = f.sa;
-            s_cf[(c * rv + r) * 2 + 1] = f.sc;
-            s_md[c * rv + r] = f.mode;
+        //     The prefix maxima come from warp scans, one warp per row and
+        //     32 chunks per step (max is exact: the grouping changes nothing).
+        for (int r = tid / 32; r < rv; r += nth / 32) {
+            const int ln = tid % 32;
+            float run = s_run[2 * r];
+            for (int cb = 0; cb < cn; cb += 32) {
+                const int c = cb + ln;
+                const float mc = c < cn ? s_ml[(c * rv + r) * 2] : -INFINITY;
+                float inc = mc;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float x = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (ln >= o)
+                        inc = fmaxf(inc, x);
+                }
+                float excl = __shfl_up_sync(0xffffffffu, inc, 1);
+                if (ln == 0)
+                    excl = -INFINITY;
+                if (c < cn) {
+                    const Fold f = fold_coef(fmaxf(run, excl), 0.f, mc, 0.f);
+                    s_cf[(c * rv + r) * 2] = f.sa;
+                    s_cf[(c * rv + r) * 2 + 1] = f.sc;
+                    s_md[c * rv + r] = f.mode;
+                }
+                run = fmaxf(run, __shfl_sync(0xffffffffu, inc, 31));
+            }
         }
         __syncthreads();
         // (c) the sequential parts, in chunk order -- the same operations
