@@ -1031,8 +1031,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             // (scale > 0, so this is the max of the scaled scores as well)
             const bool unmasked = __all_sync(0xffffffffu, nallow == HALF);
             float pmax = -INFINITY;
+            uint32_t v1[32];  // columns 32-63 of the half stay in registers for pass 2
             if (warp_active && okw) {
-                uint32_t v0[32], v1[32];
+                uint32_t v0[32];
                 tmem_ld32(scol, v0);
                 if (HALF == 64)
                     tmem_ld32(scol + 32, v1);
@@ -1091,8 +1092,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
                 for (int g2 = 0; g2 < HALF / 32; ++g2) {
                     uint32_t v[32];
-                    tmem_ld32(scol + g2 * 32, v);
-                    tmem_wait_ld();
+                    if (g2 == 0) {
+                        tmem_ld32(scol, v);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = v1[i];
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         const int c = g2 * 32 + i;
