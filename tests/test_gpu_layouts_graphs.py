@@ -131,3 +131,52 @@ def test_fused_qkv_q_stride_with_poison(qlen):
     assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
     _same_bits(out, out_r, f"fused-QKV q (q={qlen}): out")
     _same_bits(lse, lse_r, f"fused-QKV q (q={qlen}): lse")
+
+
+def test_metadata_shared_across_layers_in_one_graph():
+    """Two layers (two pools, two query sets) read one set of step metadata
+    -- block tables, lengths, query starts -- with no copy per layer
+    ("stabilize direct paged CK attention for bitwise R/R", Changes: share
+    prepared attention metadata across layers without dense KV
+    materialization).  Both prepared calls captured in one graph give each
+    layer's eager bits."""
+    w0 = wl.decode(seed=1790)
+    rows = [w0.block_table[b, :wl.pages_needed(L)].tolist() for b, L in enumerate(w0.seq_lens.tolist())]
+    w1 = wl.build("decode_second_layer", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                  seq_lens=w0.seq_lens.tolist(), query_lens=[1] * 4, num_blocks=w0.num_blocks, block_rows=rows,
+                  layout=w0.layout, seed=1791)  # same lengths and tables, other K/V and q
+    assert torch.equal(w0.block_table, w1.block_table) and not torch.equal(w0.q, w1.q)
+    layers = [DeviceWorkload(w) for w in (w0, w1)]
+    for dw in layers:
+        dw.write_cache()
+    meta = layers[0]
+    dev = meta.q.device
+    eager = [dw.attention(block_tables=meta.block_tables, seq_lens=meta.seq_lens,
+                          query_start_loc=meta.query_start_loc) for dw in layers]
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    s = torch.cuda.Stream()
+    outs = [torch.empty_like(o) for o, _ in eager]
+    lses = [torch.empty_like(l_) for _, l_ in eager]
+    ws = [pagedattn.new_workspace(4, 8, 2, 128, 1, 7168, dev) for _ in layers]
+    calls = [pagedattn.prepare_paged_attention(dw.q, dw.k_cache, dw.v_cache, meta.block_tables, meta.seq_lens,
+                                               meta.query_start_loc, dw.w.scale, 1, 7168, outs[i], lses[i], ws[i],
+                                               stream=s)
+             for i, dw in enumerate(layers)]
+    pagedattn.init()
+    with torch.cuda.stream(s):
+        for c in calls:
+            c()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for c in calls:
+            c()
+    for o in outs:
+        o.zero_()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    for i in range(2):
+        _same_bits(outs[i], eager[i][0], f"layer {i} in the shared-metadata graph: out")
+        _same_bits(lses[i], eager[i][1], f"layer {i} in the shared-metadata graph: lse")
