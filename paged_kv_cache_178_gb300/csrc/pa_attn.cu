@@ -5,7 +5,7 @@
 // query head kvh*G + hh, so the G heads sharing a KV head share every K/V
 // tile ("test(rocm): ReshapeAndCache->PagedAttention composition at real
 // dims", What changed: Hq=8, Hkv=2).  Roles (512 threads):
-//   warp 0       TMA producer: Q once, then per 128-key tile one 64-column box
+//   warp 0       TMA producer: Q once, then per KV tile one 64-column box
 //                per 16-token page for K and for V, block ids read from the
 //                request's table (and range-checked) as it goes; pages past
 //                the last needed key are never read ("fix(rocm): stabilize
@@ -25,7 +25,7 @@
 // shape, no implicit FMA contraction).  Every row follows the same sequence
 // of operations whatever the batch, query length, other rows or launch
 // bounds, so prefill and decode agree bit for bit:
-//   C1  KV tiles of 128 keys aligned to key 0; K-steps of 16 in ascending
+//   C1  KV tiles of 128 keys (64: second canon) from key 0; K-steps of 16 up
 //       order, BF16 in, FP32 accumulate (M = 128 per CTA, or 256 over a CTA
 //       pair: each output element is the same dot product either way).
 //   C2  c = scale*log2 e is formed once, in fp32, on the host (scale > 0).
@@ -34,9 +34,9 @@
 //   C3  lazy online softmax over a chunk's tiles: the reference max m moves
 //       only when a tile max exceeds m + 8 (then l and O are scaled by
 //       exp2(m_old - m_new)); p = exp2(fma(S, c, -m)) for allowed keys,
-//       exactly 0 otherwise.  Tile row sum: for each 64-column half an 8-way
-//       interleaved sum (accumulator k sums the half's columns k, k+8, ..,
-//       k+56 in order, then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))); tile sum =
+//       exactly 0 otherwise.  Tile row sum: for each half of the columns an
+//       8-way interleaved sum (accumulator k sums the half's columns k, k+8,
+//       .. in order, then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))); tile sum =
 //       half0 + half1.
 //   C4  P rounded to BF16 (RNE) before P.V.
 //   C5  head dim 128: chunks of 256 keys aligned to key 0, each starting
@@ -493,8 +493,8 @@ __device__ Unit split_unit(const AttnParams &p, int chunk, int *s_int)
 
 // PAIR: the CTAs of a two-CTA cluster take query tiles 2g (rank 0, the
 // leader) and 2g+1 of one (request, KV head) and share every MMA
-// (cta_group::2, M = 256).  Each CTA loads half of each K tile (keys 0-63 in
-// the leader, 64-127 in the other) and half of each V tile (the lower or upper
+// (cta_group::2, M = 256).  Each CTA loads half of each K tile (the leader
+// the first half of the keys) and half of each V tile (the lower or upper
 // half of the head dim), so a CTA moves half the bytes per score it computes.
 // The leader's thread issues all MMAs; tile-full barriers, P-ready and
 // fold-done barriers live in the leader, stage-release and S/PV-done commits
@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 id = 0;  // keep the pipeline flowing; the rows become NaN
             any_bad |= __any_sync(0xffffffffu, badl);
             // K boxes: (page, 64-column block) per lane; a pair member takes the
-            // pages of its 64 keys.  V boxes: all pages, this CTA's blocks.
+            // pages of its half of the keys.  V boxes: all pages, its blocks.
             const int k_page = (int)crank * (PPT / CL) + lane / NKB, k_kb = lane % NKB;
             const int k_id = __shfl_sync(0xffffffffu, id, k_page % PPT);
             const bool k_issue = lane < (PPT / CL) * NKB && k_page < np;
@@ -924,9 +924,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         auto issue_pv = [&](int j, int qk_next) -> bool {
             const int sv = j % NSV;
             const int t = t_begin + j;
-            // operands first: P of keys 0-63 sits in columns 0-31 of the S
-            // buffer, keys 64-127 in columns 64-95 (each softmax half writes
-            // its own); V advances 16 keys (2048 bytes) per instruction
+            // operands first: P of the first half of the keys sits in the first
+            // HALF/2 columns of the S buffer, the second half from column HALF
+            // (each softmax half writes its own); V: 16 keys (2 KB) per step
             const uint32_t pcol = tmem + (uint32_t)(j % NSB) * kKeys;
             const uint64_t vd0 = sdesc_sw128(smem_addr(sV + sv * VST), VBLK, 1024);
             uint32_t ad[NPV];
