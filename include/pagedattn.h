@@ -31,10 +31,13 @@
  *     failing check returns a status and launches nothing.  There is no
  *     fallback path: an unsupported shape is an error.
  *   - Device-side metadata errors (a block id outside [0, num_blocks), a slot
- *     past the pool, seq_len < query length, a non-monotone query_start_loc)
- *     never fault: the affected rows are written as NaN (attention) or
- *     skipped (cache write), other rows are untouched, and the first error
- *     is latched in a device flag read by pa_check_errors.
+ *     past the pool, seq_len < query length, a length above its bound, a
+ *     query_start_loc that decreases) never fault: the affected rows are
+ *     written as NaN (attention) or skipped (cache write), other rows are
+ *     untouched, and the first error is latched in a device flag read by
+ *     pa_check_errors.  A request whose query range is inverted
+ *     (query_start_loc[b+1] < query_start_loc[b]) owns no rows; its
+ *     neighbours are checked against the bounds with the ranges they read.
  *   - `stream` is a cudaStream_t (0 = legacy default stream).
  */
 #ifndef PAGEDATTN_H
@@ -301,6 +304,22 @@ PA_API pa_status pa_gather_kv_head(const pa_kv_cache *cache, int32_t kv_head, co
  * of the first recorded error, else -1.
  */
 PA_API pa_status pa_check_errors(pa_stream_t stream, int64_t *first_bad_index);
+
+/*
+ * Sets the time limit of the one wait in the split-KV fold that depends on
+ * other CTAs (the folders of a (request, KV head) group waiting until every
+ * CTA of the group has published its chunk state) and returns the previous
+ * limit.  The default is 2 s.  It exists to exercise the timeout path ("ROCm:
+ * harden compact peer-local KV prefill for Gemma-4", Required hardening:
+ * bounded waits, fatal after submit, no retry): with 0 the waiting CTAs give
+ * up at once, latch PA_ERR_TIMEOUT and leave their share of the rows
+ * unwritten; the kernel still ends normally.  While nothing is copied or
+ * computed at that point, no other wait is affected.  The value is read at
+ * each launch (a captured CUDA graph keeps the value of its capture) and is
+ * process-wide.  After a call that reported PA_ERR_TIMEOUT, zero-fill the
+ * workspace before reusing it.
+ */
+PA_API uint64_t pa_set_fold_wait_limit_ns(uint64_t limit_ns);
 
 /* Static, human-readable name of a status code. */
 PA_API const char *pa_status_string(pa_status status);

@@ -15,12 +15,16 @@
  *      decode ("stabilize direct paged CK attention for bitwise R/R",
  *      Additional checks: full and suffix execution, causal/LSE vs decode).
  *
- * Readings where the pages are silent (each also listed in the design notes):
- *   - query head h reads KV head h / (Hq/Hkv);
+ * Readings where the pages are silent:
+ *   - query head h reads KV head h / (Hq/Hkv) (the composition page gives
+ *     only Hq=8, Hkv=2);
  *   - seq_lens[b] counts the new tokens, so query i of request b sits at
- *     position L_b - q_b + i and may see keys 0..that position;
+ *     position L_b - q_b + i and may see keys 0..that position (the bitwise
+ *     R/R page's Operator benchmarks quote "Q128, KV7168" beside "Q1,
+ *     KV7168"; its Additional checks name full and suffix execution);
  *   - scores are scale * q.k with the fp32 scale widened to double;
- *   - LSE is the natural log of the sum of exp(scores), scale included.
+ *   - LSE is the natural log of the sum of exp(scores), scale included (the
+ *     bitwise R/R page's Additional checks name LSE without a formula).
  * There is no blocking, tiling, online rescaling or chunking here: scores
  * are materialised, the maximum taken, then the normalised sum formed.
  */

@@ -357,7 +357,7 @@ pa_status pa_reshape_and_cache(const void *key, int64_t key_tok_stride, const vo
 size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t max_query_len, int32_t max_seq_len)
 {
-    AttnPlan pl;
+    AttnPlan pl{};
     if (!plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, max_query_len, max_seq_len, &pl))
         return 0;
     return pl.ws_bytes;
@@ -370,7 +370,7 @@ pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t q_tok_
                              void *workspace, size_t workspace_bytes, pa_stream_t stream)
 {
     AttnArgs a;
-    AttnPlan pl;
+    AttnPlan pl{};
     bool empty = false;
     pa_status st = attention_check(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables,
                                    max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, max_query_len,
@@ -403,7 +403,7 @@ pa_status pa_reshape_and_paged_attention(const void *key, int64_t key_tok_stride
     if (st != PA_OK)
         return st;
     AttnArgs a;
-    AttnPlan pl;
+    AttnPlan pl{};
     bool empty = false;
     st = attention_check(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables, max_blocks_per_seq,
                          seq_lens, query_start_loc, num_seqs, max_query_len, max_seq_len, scale, out, lse,
@@ -471,13 +471,27 @@ pa_status pa_paged_attention_noalloc(const void *q, int64_t num_q_tokens, int64_
                                      int32_t max_query_len, int32_t max_seq_len, float scale, void *out,
                                      float *lse, pa_stream_t stream)
 {
-    if (!cache)
-        return PA_ERR_INVALID_ARG;
-    AttnPlan pl;
-    if (plan_attention(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_query_len, max_seq_len,
-                       &pl) &&
-        pl.ws_bytes > PA_NOALLOC_SCRATCH_BYTES)
-        return PA_ERR_WORKSPACE;  // these bounds need more scratch than the built-in array holds
+    // Every host check of pa_paged_attention runs first, against the
+    // built-in array's size, before any CUDA call: a stand-in address (256,
+    // aligned and never dereferenced) takes the scratch's place until the
+    // call is known to be valid.  Bounds that need more scratch than the
+    // array holds fail here with PA_ERR_WORKSPACE.
+    AttnArgs a;
+    AttnPlan pl{};
+    bool empty = false;
+    pa_status st = attention_check(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables,
+                                   max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, max_query_len,
+                                   max_seq_len, scale, out, lse, reinterpret_cast<void *>(uintptr_t{256}),
+                                   PA_NOALLOC_SCRATCH_BYTES, &a, &pl, &empty);
+    if (st != PA_OK)
+        return st;
+    if (empty) {
+        snprintf(g_last_info, sizeof g_last_info, "attention: empty batch (nothing launched)");
+        return PA_OK;
+    }
+    ErrState *err = nullptr;
+    if ((st = device_setup(&err)) != PA_OK)
+        return st;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return PA_ERR_CUDA;
@@ -494,15 +508,17 @@ pa_status pa_paged_attention_noalloc(const void *q, int64_t num_q_tokens, int64_
         }
         scratch = g_noalloc_ptr[dev];
     }
+    a.workspace = scratch;
+    a.workspace_bytes = PA_NOALLOC_SCRATCH_BYTES;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The arrival counters at the head of the scratch must start at zero; the
     // previous call (or an aborted one) may have left anything there.
-    if (pl.ws_counter_bytes > 0 &&
-        cudaMemsetAsync(scratch, 0, pl.ws_counter_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (pl.ws_counter_bytes > 0 && cudaMemsetAsync(scratch, 0, pl.ws_counter_bytes, s) != cudaSuccess)
         return PA_ERR_CUDA;
-    return pa_paged_attention(q, num_q_tokens, q_tok_stride, num_q_heads, cache, block_tables, max_blocks_per_seq,
-                              seq_lens, query_start_loc, num_seqs, max_query_len, max_seq_len, scale, out, lse,
-                              scratch, PA_NOALLOC_SCRATCH_BYTES, stream);
+    return attention_launch(a, pl, err, s, g_last_info, sizeof g_last_info);
 }
+
+uint64_t pa_set_fold_wait_limit_ns(uint64_t limit_ns) { return set_fold_wait_limit_ns(limit_ns); }
 
 pa_status pa_check_errors(pa_stream_t stream, int64_t *first_bad_index)
 {

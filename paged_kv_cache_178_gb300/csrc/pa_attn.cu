@@ -45,6 +45,8 @@
 //       Head dim 256: one chunk (no split).
 //   C6  out = O * rcp_rn(l) -> BF16 RNE; lse = (m + log2 l) * ln 2.
 #include <cuda_bf16.h>
+
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -200,9 +202,11 @@ __device__ __forceinline__ void split_arrive_and_merge(const AttnParams &p, int6
             // narrive every partial record is visible (the acquire reads the
             // end of the release sequence formed by the arrivals)
             if (merger < K - 1) {
+                // bounded by p.fold_wait_ns; a limit of 0 gives up without
+                // polling (nothing is in flight here: no copy, no MMA)
                 const uint64_t t0 = global_timer_ns();
-                while (ld_acquire_u32(p.ws_cnt + unit_q) < (uint32_t)narrive) {
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                while (p.fold_wait_ns == 0 || ld_acquire_u32(p.ws_cnt + unit_q) < (uint32_t)narrive) {
+                    if (p.fold_wait_ns == 0 || global_timer_ns() - t0 > p.fold_wait_ns) {
                         record_error(p.err, kErrTimeout, ((long long)blockIdx.x << 8) | 0xFF);
                         merger = -1;
                         break;
@@ -1383,6 +1387,14 @@ cudaError_t init_attention_attributes()
     return init_attention512_attributes();
 }
 
+// Limit of the split-KV fold's cross-CTA wait, read at each launch (a
+// captured graph keeps the value it was captured with).
+static std::atomic<uint64_t> g_fold_wait_ns{kWaitLimitNs};
+
+uint64_t fold_wait_limit_ns() { return g_fold_wait_ns.load(std::memory_order_relaxed); }
+
+uint64_t set_fold_wait_limit_ns(uint64_t ns) { return g_fold_wait_ns.exchange(ns, std::memory_order_relaxed); }
+
 // SM count of the current device, looked up once per device.
 static int num_sms_of_current_device()
 {
@@ -1452,6 +1464,7 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.num_sms = num_sms_of_current_device();
     p.cpu = pl.cpu;
     p.early_reads = a.early_reads ? 1 : 0;
+    p.fold_wait_ns = fold_wait_limit_ns();
     // C2: scale * log2(e) formed once, in fp32, on the host
     p.scale_log2 = a.scale * 1.4426950408889634f;
     cudaLaunchConfig_t cfg = {};

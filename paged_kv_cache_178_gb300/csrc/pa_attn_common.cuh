@@ -40,6 +40,7 @@ struct AttnParams {
     int32_t early_reads;  // only the K/V copies wait for the preceding grid
     int32_t num_sms;      // SMs of the device (split-KV: whether every unit is resident)
     int32_t cpu;          // split-KV: consecutive chunks per CTA (each still writes one record per chunk)
+    uint64_t fold_wait_ns;  // limit of the split-KV fold's cross-CTA wait (0: give up at once)
     float scale_log2;
 };
 

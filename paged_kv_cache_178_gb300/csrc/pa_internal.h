@@ -62,7 +62,7 @@ struct AttnPlan {
     int nch;            // grid extent over KV chunks (1 unless split)
     bool split;         // split-KV with partial states + in-kernel merge
     int cpu;            // split-KV: consecutive chunks per CTA (>= 1)
-    int cl;             // CTAs per cluster multicasting K/V tiles (in-CTA schedule)
+    int cl;             // CTAs per cluster (2: a CTA pair shares each MMA, in-CTA schedule)
     int ws_rows;        // rows per partial-state record
     size_t ws_counter_bytes;
     size_t ws_bytes;    // total workspace needed
@@ -79,6 +79,11 @@ cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &plan, ErrState *
                              cudaStream_t stream, char *info, size_t info_len);
 
 cudaError_t init_attention_attributes();
+
+// Limit (ns) of the split-KV fold's cross-CTA wait; the setter returns the
+// previous value.
+uint64_t fold_wait_limit_ns();
+uint64_t set_fold_wait_limit_ns(uint64_t ns);
 
 // Head dim 512: two-CTA clusters (pa_attn512.cu).
 cudaError_t init_attention512_attributes();

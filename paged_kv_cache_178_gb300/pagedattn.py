@@ -37,7 +37,7 @@ PA_ERR_CUDA = 6
 
 EXPORTED = ("pa_init", "pa_reshape_and_cache", "pa_paged_attention_workspace_size",
             "pa_paged_attention", "pa_paged_attention_noalloc", "pa_reshape_and_paged_attention",
-            "pa_gather_kv_head", "pa_check_errors",
+            "pa_gather_kv_head", "pa_check_errors", "pa_set_fold_wait_limit_ns",
             "pa_status_string", "pa_last_launch_info")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -92,6 +92,8 @@ def load(path: str = LIB_PATH):
                                           vp, vp]
         lib.pa_check_errors.restype = i32
         lib.pa_check_errors.argtypes = [vp, ctypes.POINTER(i64)]
+        lib.pa_set_fold_wait_limit_ns.restype = ctypes.c_uint64
+        lib.pa_set_fold_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_status_string.argtypes = [i32]
         lib.pa_last_launch_info.restype = None
@@ -116,6 +118,13 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
 
 def init() -> None:
     _check(load().pa_init(), "pa_init")
+
+
+def set_fold_wait_limit_ns(limit_ns: int) -> int:
+    """Time limit of the split-KV fold's cross-CTA wait (default 2 s); returns
+    the previous limit.  0 makes the waiting CTAs give up at once (a test of
+    the timeout path)."""
+    return int(load().pa_set_fold_wait_limit_ns(int(limit_ns)))
 
 
 def last_launch_info() -> str:

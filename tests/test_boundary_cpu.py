@@ -203,3 +203,33 @@ def test_gather_validation_and_overlap(lib):
         assert _gkv(lib, c) == pagedattn.PA_ERR_CUDA
         assert _gkv(lib, c, pv=_BUF["out"] + 1800 * 4096) == pagedattn.PA_ERR_CUDA  # adjacent: fine
         assert _gkv(lib, c, cap=0, pk=0, pv=0) == pagedattn.PA_ERR_CUDA  # offsets only
+
+
+def _noalloc(lib, cache, q=FAKE, ntok=4, qstride=1024, hq=8, bt=FAKE, maxblk=448, sl=FAKE, qsl=FAKE,
+             nseq=4, mq=1, ms=7168, scale=0.088, out=FAKE, lse=0):
+    return lib.pa_paged_attention_noalloc(q, ntok, qstride, hq, ctypes.byref(cache), bt, maxblk, sl, qsl,
+                                          nseq, mq, ms, ctypes.c_float(scale), out, lse, None)
+
+
+def test_noalloc_validates_before_any_cuda_call(lib):
+    """The allocation-free entry point runs every host check of the regular
+    one, against its built-in scratch size, before it touches CUDA: on a
+    machine without a GPU a bad call returns its own status, and only a
+    valid call reaches the CUDA runtime (PA_ERR_CUDA here)."""
+    import torch
+    c = _cache()
+    assert _noalloc(lib, c, hq=7) == pagedattn.PA_ERR_UNSUPPORTED               # Hq % Hkv
+    assert _noalloc(lib, _cache(head_dim=64)) == pagedattn.PA_ERR_UNSUPPORTED    # head dim
+    assert _noalloc(lib, _cache(num_kv_heads=0)) == pagedattn.PA_ERR_INVALID_ARG
+    assert _noalloc(lib, c, mq=-1) == pagedattn.PA_ERR_INVALID_ARG
+    assert _noalloc(lib, c, q=0) == pagedattn.PA_ERR_INVALID_ARG
+    assert _noalloc(lib, c, out=FAKE + 8) == pagedattn.PA_ERR_INVALID_ARG
+    assert _noalloc(lib, c, scale=0.0) == pagedattn.PA_ERR_INVALID_ARG
+    assert lib.pa_paged_attention_noalloc(FAKE, 4, 1024, 8, None, FAKE, 448, FAKE, FAKE, 4, 1, 7168,
+                                          ctypes.c_float(0.088), FAKE, 0, None) == pagedattn.PA_ERR_INVALID_ARG
+    big = 1 << 20                      # bounds whose scratch exceeds the built-in array
+    assert pagedattn.workspace_size(4, 8, 2, 128, 1, big) > pagedattn.NOALLOC_SCRATCH_BYTES
+    assert _noalloc(lib, c, ms=big) == pagedattn.PA_ERR_WORKSPACE
+    assert _noalloc(lib, c, nseq=0) == pagedattn.PA_OK                          # empty batch
+    if not torch.cuda.is_available():
+        assert _noalloc(lib, c) == pagedattn.PA_ERR_CUDA                        # valid: reaches CUDA

@@ -350,16 +350,63 @@ def test_bound_violation_flags():
 
 # ------------------------------------------------------- head dim 512 ----
 
-@pytest.mark.parametrize("L", [3072, 18432])
+@pytest.mark.parametrize("L", list(wl.WIDE_LENS))
 def test_wide_head_dh512(L):
-    """Hq=16, Hkv=2, d=512 causal prefill (two-CTA pairs split the head dim)."""
+    """Hq=16, Hkv=2, d=512 causal prefill (two-CTA pairs split the head dim)
+    at every stated length ("harden compact peer-local KV prefill for
+    Gemma-4", Gates: ~3k / ~11k / ~18k; Scope: 8192), on sampled rows that
+    include the first and last row of a page, of a 64-key tile and of a
+    1024-key span, and the last row."""
     w = wl.wide_head(L)
     dw, out, lse = _run(w)
     assert "in-cta-pair" in pagedattn.last_launch_info()
-    rows = _rows_sample(L, extra=(63, 64, 65, L // 2), k=24 if L > 8192 else 48)
+    rows = _rows_sample(L, extra=(15, 16, 63, 64, 65, 127, 128, 1023, 1024, L // 2, L - 1),
+                        k=24 if L > 8192 else 48)
     _compare(w, out, lse, rows=rows)
 
 
-def test_wide_head_prefill_equals_decode():
-    w = wl.wide_head(3072)
-    _prefill_vs_decode(w, [0, 15, 16, 63, 64, 1000, 2047, 3071])
+@pytest.mark.parametrize("L,nrows", [(3072, 24), (18432, 72)])
+def test_wide_head_prefill_equals_decode(L, nrows):
+    """Dh=512 prefill rows equal their decode view bit for bit, up to the
+    last row of the longest stated length."""
+    w = wl.wide_head(L)
+    fixed = {0, 15, 16, 63, 64, 127, 128, 1000, 1023, 1024, 2047, L // 2, L - 2, L - 1}
+    g = torch.Generator().manual_seed(L)
+    rand = set(torch.randint(0, L, (nrows,), generator=g).tolist())
+    rows = sorted(fixed | rand)[:max(nrows, len(fixed))]
+    rows = sorted(set(rows) | fixed)
+    assert len(rows) >= min(nrows, L) and rows[-1] == L - 1
+    _prefill_vs_decode(w, rows)
+
+
+def test_composition_prefill_equals_decode_all_rows():
+    """The Dh=256 composition (20 tokens, table {3,1,2,0}): each of the 20
+    prefill rows equals its decode view bit for bit."""
+    _prefill_vs_decode(wl.composition(), list(range(20)))
+
+
+# ----------------------------------------------- non-monotone query starts ----
+
+@pytest.mark.parametrize("qsl_bad,bad_rows,bad_reqs", [
+    ([0, 1, 3, 2, 4], [1, 2, 3], {1, 2, 3}),   # an inner entry decreases
+    ([0, 1, 2, 4, 3], [2, 3], {2, 3}),         # the last step decreases
+])
+def test_non_monotone_query_start_loc(qsl_bad, bad_rows, bad_reqs):
+    """A query_start_loc that decreases is invalid metadata: the request whose
+    range is inverted owns no rows, the requests whose ranges now exceed the
+    query bound get NaN rows, PA_ERR_BAD_METADATA names one of them, and the
+    rows of the requests left intact keep every bit."""
+    w = wl.decode()
+    dw, out, lse = _run(w)
+    qsl = torch.tensor(qsl_bad, dtype=torch.int32, device=out.device)
+    o2 = torch.zeros_like(out)
+    l2 = torch.zeros_like(lse)
+    dw.attention(query_start_loc=qsl, out=o2, lse=l2)
+    st, idx = pagedattn.check_errors()
+    print(f"qsl={qsl_bad}: status={pagedattn.status_string(st)} index={idx}")
+    assert st == pagedattn.PA_ERR_BAD_METADATA and idx in bad_reqs
+    for r in bad_rows:
+        assert torch.isnan(o2[r].float()).all() and torch.isnan(l2[r]).all()
+    keep = [r for r in range(4) if r not in bad_rows]
+    _bitwise(out[keep], o2[keep], f"rows {keep} beside a non-monotone query_start_loc")
+    _bitwise(lse[keep], l2[keep], "their lse")
