@@ -16,8 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedattn.so")
-SOURCES = ["pa_api.cu", "pa_attn.cu", "pa_attn512.cu", "pa_gather.cu"]
-HEADERS = ["pa_internal.h", "pa_ptx.cuh", "pa_attn_common.cuh", os.path.join("..", "..", "include", "pagedattn.h")]
+SOURCES = ["pa_api.cu", "pa_attn.cu", "pa_attn512.cu", "pa_decode.cu", "pa_gather.cu"]
+HEADERS = ["pa_internal.h", "pa_ptx.cuh", "pa_attn_common.cuh", "pa_split.cuh", os.path.join("..", "..", "include", "pagedattn.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no implicit FMA contraction, so the softmax/rescale order is

@@ -1,0 +1,118 @@
+"""Decode with few query rows per (request, KV head): the head-dim-128 kernel
+that swaps the MMA operands (keys on the tensor-memory lanes) for query
+tiles of up to 32 rows, in every row-count variant (4, 8, 16, 32 rows), on
+the split-KV and the single-CTA schedules.
+
+Each case is checked against the fp64 oracle (max-abs 2e-2, lse relative
+1e-3) and bit for bit against the same rows computed by a full causal
+prefill of the request, which runs the 128-row kernel ("fix(rocm): stabilize
+direct paged CK attention for bitwise R/R", Validation: prefill and decode
+agree bitwise; Changes: one query per decode row)."""
+import pytest
+import torch
+
+from paged_kv_cache_178_gb300 import pagedattn
+from paged_kv_cache_178_gb300 import workloads as wl
+from paged_kv_cache_178_gb300.device import DeviceWorkload
+from tests.helpers import LSE_RTOL, OUT_ATOL, lse_rel_err, oracle_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def _bitwise(a, b, what):
+    ai = a.contiguous().view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32)
+    bi = b.contiguous().view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)
+    mism = int((ai != bi).sum())
+    print(f"{what}: mismatch_count={mism}")
+    assert mism == 0
+
+
+def _suffix_batch(hq, hkv, lens, qlens, seed):
+    gen = torch.Generator().manual_seed(seed)
+    nb = sum(wl.pages_needed(L) for L in lens) + 16
+    pages = torch.randperm(nb, generator=gen).tolist()
+    rows, at = [], 0
+    for L in lens:
+        n = wl.pages_needed(L)
+        rows.append(pages[at:at + n])
+        at += n
+    return wl.build(f"suffix_hq{hq}_hkv{hkv}_q{max(qlens)}", num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                    seq_lens=lens, query_lens=qlens, num_blocks=nb, block_rows=rows, layout="interleaved",
+                    seed=seed)
+
+
+@pytest.mark.parametrize("hq,hkv,qlens,expect_rows", [
+    (8, 2, [1, 1, 1, 1], 4),          # decode, G = 4
+    (8, 2, [2, 1, 2, 1], 8),          # two-token speculative steps
+    (8, 2, [4, 3, 1, 2], 16),
+    (8, 2, [8, 5, 1, 7], 32),
+    (16, 2, [1, 2, 3, 4], 32),        # G = 8
+    (2, 2, [3, 1, 4, 2], 4),          # G = 1
+    (32, 2, [1, 1, 1, 1], 16),        # G = 16
+])
+def test_few_row_decode_matches_oracle_and_prefill(hq, hkv, qlens, expect_rows):
+    lens = [4171, 513, 300, 1000]
+    w = _suffix_batch(hq, hkv, lens, qlens, seed=90 + hq + sum(qlens))
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    print(info)
+    assert f"decode-swapped-r{expect_rows}" in info and "split" in info
+    ref_o, ref_l = oracle_attention(w)
+    err_o = float((out.float().cpu().double() - torch.from_numpy(ref_o)).abs().max())
+    err_l = lse_rel_err(lse.cpu().numpy(), ref_l)
+    print(f"oracle: out max_abs_diff={err_o:.3e} lse rel={err_l:.3e}")
+    assert err_o <= OUT_ATOL and err_l <= LSE_RTOL
+    # each request's rows against a full prefill of that request (the
+    # 128-row kernel), bit for bit
+    for b in range(len(lens)):
+        L, qn = lens[b], qlens[b]
+        kv0 = sum(lens[:b])
+        q0 = int(w.query_start_loc[b])
+        wp = wl.build("prefill_view", num_q_heads=hq, num_kv_heads=hkv, head_dim=128, seq_lens=[L],
+                      query_lens=[L], num_blocks=w.num_blocks, block_rows=[w.block_table[b].tolist()],
+                      layout=w.layout, seed=1)
+        # the prefill view reads the decode workload's cache: its q rows are
+        # replaced by the decode q where the decode has them
+        qp = torch.zeros((L, hq, 128), dtype=torch.bfloat16)
+        qp[L - qn:] = w.q[q0:q0 + qn]
+        dp = DeviceWorkload(wp, fill_bits=None, with_workspace=False)
+        dp.share_cache_with(dw)
+        dp.q = qp.cuda()
+        dp.max_query_len = L
+        dp.max_seq_len = L
+        op, lp = dp.attention()
+        assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+        assert "decode-swapped" not in pagedattn.last_launch_info()
+        _bitwise(out[q0:q0 + qn], op[L - qn:], f"request {b} (q={qn}) decode vs prefill")
+        _bitwise(lse[q0:q0 + qn], lp[L - qn:], f"request {b} lse")
+
+
+def test_single_cta_schedule_equals_split():
+    """Enough requests that every (request, KV head) gets one CTA that folds
+    its chunks itself (no split-KV records); each request alone runs the
+    split schedule.  Both give the same bits."""
+    lens = [1000 + 37 * i for i in range(80)]
+    w = wl.decode(seq_lens=lens, num_blocks=sum(wl.pages_needed(L) for L in lens) + 8)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    assert "decode-swapped-r4" in info and "split" not in info, info
+    dev = out.device
+    for b in (0, 17, 79):
+        o1, l1 = dw.attention(q=dw.q[b:b + 1], block_tables=dw.block_tables[b:b + 1].contiguous(),
+                              seq_lens=dw.seq_lens[b:b + 1].contiguous(),
+                              query_start_loc=torch.tensor([0, 1], dtype=torch.int32, device=dev),
+                              max_seq_len=int(w.seq_lens[b]))
+        assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+        assert "split" in pagedattn.last_launch_info()
+        _bitwise(out[b:b + 1], o1, f"request {b}: single-CTA fold vs split-KV merge")
+        _bitwise(lse[b:b + 1], l1, f"request {b} lse")
+    ref_o, ref_l = oracle_attention(w, rows=[0, 17, 79])
+    o = out.float().cpu().double()[[0, 17, 79]]
+    assert float((o - torch.from_numpy(ref_o)).abs().max()) <= OUT_ATOL
+    assert lse_rel_err(lse.cpu().numpy()[[0, 17, 79]], ref_l) <= LSE_RTOL
