@@ -37,7 +37,10 @@
 //                a shared-memory copy of p, P^T written to shared memory.
 //   warps 8-11   chunk epilogue: thread d = head-dim element d (TMEM lane d):
 //                chunk records (split-KV) or the in-CTA fold and the output.
-//   all          the unit scan before, the split-KV arrival and merge after.
+//   all          the unit scan before; in the last-arriving CTA of a split-KV
+//                group, the fold of the group's chunk records after.
+// Split-KV: the epilogue warps arrive on the group's counter as soon as
+// their chunk records are written; the last arrival folds (no CTA waits).
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -136,6 +139,196 @@ __device__ __forceinline__ void tmem_st_r(uint32_t taddr, const uint32_t (&r)[R]
 
 }  // namespace dec
 
+// Split-KV arrival, by the four epilogue warps (thread t = 0..127) right
+// after they wrote this CTA's chunk records: an acquire-release add on the
+// (request, KV head) group's counter.  The last CTA of the group to arrive
+// folds (dec_merge); the others leave at once, so no CTA ever waits for
+// another.  *s_flag = 1 in the folding CTA.
+__device__ __forceinline__ void dec_arrive(const AttnParams &p, int64_t unit_q, int narrive, int *s_flag)
+{
+    const int t = threadIdx.x - 256;
+    named_sync(3, 128);  // every record of this CTA is written (each thread's stores precede the barrier)
+    if (t == 0) {
+        // releases this CTA's records and, for the last arrival, acquires
+        // every other CTA's
+        uint32_t old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + unit_q) : "memory");
+        const bool last = old == (uint32_t)(narrive - 1);  // above: a counter left by a failed call, fold nothing
+        if (last)
+            p.ws_cnt[unit_q] = 0u;  // ready for the next call
+        *s_flag = last ? 1 : 0;
+    }
+}
+
+// The fold of a group's chunk records, left to right (C5), and the output
+// (C6), by every thread of the last-arriving CTA after the CTA barrier that
+// follows dec_arrive (which orders the acquire before these loads).  It is the
+// in-CTA fold's sequence of fold_coef / fold_elem steps, computed per segment
+// of records staged in shared memory: first the factors and mode of every
+// (chunk, row) from the running maximum before the chunk (fold_coef's m is
+// max(m_acc, m_chunk) in every mode and max is exact, so a warp scan gives
+// it), then the l chains (last warp, one row per thread) beside the O chains
+// (the other warps, one warp per row, four consecutive elements per thread,
+// four chunks' operands loaded ahead of their steps).
+template <int R>
+__device__ __forceinline__ void dec_merge(const AttnParams &p, int64_t unit_q, int nchunks, int rv, int64_t tok_first,
+                                          int kvh, float *work, int work_floats)
+{
+    constexpr int DH = dec::DH;
+    constexpr int NTH = dec::kThreads;
+    const int tid = threadIdx.x, warp = tid / 32, ln = tid % 32;
+    const int Rw = p.ws_rows;
+    const int64_t hdr = part_header_floats(Rw);
+    const int64_t ustride = part_record_floats(Rw, DH);
+    const float *part0 = p.ws_part + unit_q * p.nch * ustride;
+    // staging area after a fixed head: [32] running max per row, [64] final (m, l)
+    float *s_carry = work, *s_fin = work + 32;
+    float *stage = work + 96;
+    // per segment: m[cn][rv], l[cn][rv] (each padded to 4 floats), O[cn][rv][DH],
+    // factors {sa, sc}[cn][rv], mode[cn][rv]
+    const int per_chunk = rv * (DH + 5);
+    const int seg = max(1, (work_floats - 96 - 16) / per_chunk);
+    if (tid < 32)
+        s_carry[tid] = -INFINITY;
+    // O chains: warp w (w < NOW) takes rows w, w + NOW, ..; lane l takes the
+    // head-dim elements 4l .. 4l+3 of its row (one 16-byte load per chunk)
+    constexpr int NOW = NTH / 32 - 1;             // O-chain warps (the last warp runs the l chains)
+    constexpr int NPR = (R + NOW - 1) / NOW;      // rows per O-chain warp
+    float4 ov[NPR];
+#pragma unroll
+    for (int q = 0; q < NPR; ++q)
+        ov[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l_run = 0.f;
+    for (int c0 = 0; c0 < nchunks; c0 += seg) {
+        const int cn = min(seg, nchunks - c0);
+        const int hdr4 = (cn * rv + 3) & ~3;
+        float *s_m = stage, *s_l = s_m + hdr4, *s_o = s_l + hdr4;
+        float2 *s_cf = reinterpret_cast<float2 *>(s_o + cn * rv * DH);
+        int *s_md = reinterpret_cast<int *>(s_cf + cn * rv);
+        // (a) stage the segment's records: every copy in flight at once
+        for (int i = tid; i < cn * rv * 2; i += NTH) {
+            const int c = i / (2 * rv), k = i % (2 * rv), which = k / rv, n = k % rv;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr((which ? s_l : s_m) + c * rv + n)),
+                         "l"(part0 + (c0 + c) * ustride + which * Rw + n)
+                         : "memory");
+        }
+        for (int i = tid; i < cn * rv * (DH / 4); i += NTH) {
+            const int c = i / (rv * (DH / 4)), k = i % (rv * (DH / 4)), n = k / (DH / 4), v4 = k % (DH / 4);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(s_o + (c * rv + n) * DH + 4 * v4)),
+                         "l"(part0 + (c0 + c) * ustride + hdr + (int64_t)n * DH + 4 * v4)
+                         : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+        // (b) factors and mode of every (chunk, row), one warp per row, 32 chunks per step
+        for (int n = warp; n < rv; n += NTH / 32) {
+            float run = s_carry[n];
+            for (int cb = 0; cb < cn; cb += 32) {
+                const int c = cb + ln;
+                const float mc = c < cn ? s_m[c * rv + n] : -INFINITY;
+                float inc = mc;
+#pragma unroll
+                for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                    const float x = __shfl_up_sync(0xffffffffu, inc, o2);
+                    if (ln >= o2)
+                        inc = fmaxf(inc, x);
+                }
+                float excl = __shfl_up_sync(0xffffffffu, inc, 1);
+                if (ln == 0)
+                    excl = -INFINITY;
+                if (c < cn) {
+                    const Fold f = fold_coef(fmaxf(run, excl), 0.f, mc, 0.f);
+                    s_cf[c * rv + n] = make_float2(f.sa, f.sc);
+                    s_md[c * rv + n] = f.mode;
+                }
+                run = fmaxf(run, __shfl_sync(0xffffffffu, inc, 31));
+            }
+            __syncwarp();
+            if (ln == 0)
+                s_carry[n] = run;
+        }
+        __syncthreads();
+        if (warp == NOW) {
+            // (c) the l chain of row ln: fold_coef's l, in chunk order
+            const int n = ln;
+            if (n < rv) {
+                for (int cb = 0; cb < cn; cb += 7) {
+                    float lc[7];
+                    float2 cf[7];
+                    int md[7];
+#pragma unroll
+                    for (int k = 0; k < 7; ++k) {
+                        const int i = min(cb + k, cn - 1) * rv + n;
+                        lc[k] = s_l[i];
+                        cf[k] = s_cf[i];
+                        md[k] = cb + k < cn ? s_md[i] : 0;  // past the last chunk: keep
+                    }
+#pragma unroll
+                    for (int k = 0; k < 7; ++k) {
+                        const float l2 = __fadd_rn(__fmul_rn(l_run, cf[k].x), __fmul_rn(lc[k], cf[k].y));
+                        l_run = md[k] == 1 ? lc[k] : (md[k] == 2 ? l2 : l_run);
+                    }
+                }
+            }
+        } else {
+            // (d) the O chains: per chunk one 16-byte load of the row's four
+            //     elements, the row's factors and mode (broadcast), four steps
+#pragma unroll
+            for (int q = 0; q < NPR; ++q) {
+                const int n = warp + q * NOW;
+                if (n < rv) {
+                    float4 a = ov[q];
+                    for (int cb = 0; cb < cn; cb += 4) {
+                        float4 x[4];
+                        float2 f[4];
+                        int md[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int c = min(cb + k, cn - 1);
+                            x[k] = reinterpret_cast<const float4 *>(s_o + (c * rv + n) * DH)[ln];
+                            f[k] = s_cf[c * rv + n];
+                            md[k] = cb + k < cn ? s_md[c * rv + n] : 0;  // past the last chunk: keep
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            a.x = fold_elem_sel(a.x, x[k].x, f[k].x, f[k].y, md[k]);
+                            a.y = fold_elem_sel(a.y, x[k].y, f[k].x, f[k].y, md[k]);
+                            a.z = fold_elem_sel(a.z, x[k].z, f[k].x, f[k].y, md[k]);
+                            a.w = fold_elem_sel(a.w, x[k].w, f[k].x, f[k].y, md[k]);
+                        }
+                    }
+                    ov[q] = a;
+                }
+            }
+        }
+        __syncthreads();  // the next segment reuses the staging area
+    }
+    // (e) epilogue (C6)
+    if (warp == NOW && ln < rv) {
+        s_fin[2 * ln] = s_carry[ln];
+        s_fin[2 * ln + 1] = l_run;
+    }
+    __syncthreads();
+    const int G = p.group;
+    if (warp < NOW) {
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) {
+            const int n = warp + q * NOW;
+            if (n < rv) {
+                const int64_t tok = tok_first + n / G;
+                const int head = kvh * G + n % G;
+                const float ln_ = s_fin[2 * n + 1];
+                const float r = __frcp_rn(ln_);
+                const uint32_t lo = pack_bf16x2(__fmul_rn(ov[q].x, r), __fmul_rn(ov[q].y, r));
+                const uint32_t hi = pack_bf16x2(__fmul_rn(ov[q].z, r), __fmul_rn(ov[q].w, r));
+                *reinterpret_cast<uint2 *>(p.out + (tok * p.hq + head) * DH + 4 * ln) = make_uint2(lo, hi);
+                if (ln == 0 && p.lse)
+                    p.lse[tok * p.hq + head] = lse_of(s_fin[2 * n], ln_);
+            }
+        }
+    }
+}
+
 // R: query rows the CTA processes (a power of two >= the request's query
 // tokens times G); NR = max(R, 16) is the N of both swapped MMAs.  Rows are
 // token-major: row n = t*G + hh is query token t of the request, head kvh*G+hh.
@@ -189,11 +382,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1) dec_kernel(const __grid_cons
     const int warp = tid / 32, lane = tid % 32;
     float *const merge_work = reinterpret_cast<float *>(sK);
     constexpr int kMergeWorkFloats = (NSK * KST + NSV * KST) / 4;
-    static_assert(kMergeWorkFloats >= R * DH + 4 * R + R * (DH + 5) + 16, "merge staging");
+    static_assert(kMergeWorkFloats >= R * (DH + 5) + 96 + 16 + 8, "merge staging: one chunk of R rows");
 
     // ---------------------------------------------------------- work unit --
     int b, kvh, c_grid = 0;
-    bool split_multi = false;
     ReqMeta meta;
     if (p.split) {
         const Unit un = split_unit(p, kChunk, reinterpret_cast<int *>(s_xmax));
@@ -203,7 +395,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1) dec_kernel(const __grid_cons
         kvh = un.kvh;
         c_grid = un.c;
         meta = un.meta;
-        split_multi = un.total <= p.num_sms;
     } else {
         const long long u = blockIdx.x;
         kvh = (int)(u % p.hkv);
@@ -719,6 +910,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1) dec_kernel(const __grid_cons
             if (lane == 0)
                 mbar_arrive(bar(B_OF + (k & 1)));
         }
+        // Split-KV: arrive as soon as the records are written (also after a
+        // failed wait, so the group's count completes)
+        if (p.split)
+            dec_arrive(p, unit_q, (nchunks + p.cpu - 1) / p.cpu, &sflags[2]);
     }
 
     tc_fence_before();
@@ -727,9 +922,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1) dec_kernel(const __grid_cons
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (p.split)
-        split_arrive_and_merge<DH>(p, unit_q, nchunks, (nchunks + p.cpu - 1) / p.cpu, rv, tok_first, kvh,
-                                   merge_work, kMergeWorkFloats, &sflags[2], split_multi);
+    // The last arrival folds, with every thread: all of this CTA's MMAs and
+    // copies have completed, so the K/V stage area is free.
+    if (p.split && sflags[2])
+        dec_merge<R>(p, unit_q, nchunks, rv, tok_first, kvh, merge_work, kMergeWorkFloats);
 }
 
 // ------------------------------------------------------------------ host --

@@ -251,23 +251,29 @@ def test_batch_composition_and_order_do_not_change_bits():
         _bitwise(lse[b:b + 1], l1, f"request {b} alone (lse)")
 
 
-def test_shared_fold_equals_single_fold():
-    """Split-KV decode: when every unit of the grid is resident at once, the
-    last four arrivals of a (request, KV head) group share the chunk fold by
-    columns; in a grid with more units than SMs the last arrival folds alone.
-    A request's bits must not depend on which of the two ran."""
+@pytest.mark.parametrize("kv_tile", [0, 64])
+def test_shared_fold_equals_single_fold(kv_tile):
+    """Split-KV decode on a big batch (more units than SMs) and on one request
+    of it alone.  In the 128-row kernel (the 64-key canon takes it) the two
+    fold differently: with every unit resident the last four arrivals of a
+    (request, KV head) group share the chunk fold by columns, otherwise the
+    last arrival folds alone; the few-row decode kernel always folds in the
+    last arrival.  A request's bits must not depend on the batch."""
     lens = [7168] + [1024] * 40
     w = wl.decode(seq_lens=lens, num_blocks=4096)
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
     units = 2 * sum((L + 255) // 256 for L in lens)
     assert units > n_sms  # the whole batch folds with one CTA per group
-    dw, out, lse = _run(w)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention(kv_tile=kv_tile)
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
     assert "split" in pagedattn.last_launch_info()
     dev = out.device
     o1, l1 = dw.attention(q=dw.q[0:1], block_tables=dw.block_tables[0:1].contiguous(),
                           seq_lens=dw.seq_lens[0:1].contiguous(),
                           query_start_loc=torch.tensor([0, 1], dtype=torch.int32, device=dev),
-                          max_seq_len=7168)
+                          max_seq_len=7168, kv_tile=kv_tile)
     assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
     assert "split" in pagedattn.last_launch_info()
     assert 2 * 28 <= n_sms  # request 0 alone: 56 units, the fold is shared
