@@ -50,7 +50,7 @@ from paged_kv_cache_178_gb300 import workloads as wl  # noqa: E402
 METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s, % of GB300 roofline"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_kernel_decode_b4_kv7168.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_178_gb300", "csrc", f)
-                  for f in ("pa_attn.cu", "pa_attn_common.cuh", "pa_ptx.cuh")]
+                  for f in ("pa_decode.cu", "pa_split.cuh", "pa_attn_common.cuh", "pa_ptx.cuh")]
 
 
 def kernel_source_hash() -> str:
@@ -440,7 +440,7 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": profile_traffic(),
-                     "kernel": "attn_kernel<128> (split-KV decode)",
+                     "kernel": "dec_kernel<4> (split-KV decode, keys on the tensor-memory lanes)",
                      "bytes_per_launch": attn_bytes, "us_per_launch": round(t_attn * 1e6, 3),
                      "peak_source": f"{peak_src} hbm_gbs"},
         "clocks": clocks,
