@@ -58,7 +58,11 @@ constexpr int DH = 128;
 constexpr int kKeys = 128;                // C1
 constexpr int kChunk = 256;               // C5 at head dim 128
 constexpr int TPC = kChunk / kKeys;       // tiles per chunk
-constexpr int NSK = 3, NSV = 2;           // K and V stages
+constexpr int NSK = 3;                    // K stages
+// V stages: three where shared memory allows (up to 16 rows), so the copy of
+// V(j) can start once P.V(j-3) has finished rather than P.V(j-2)
+template <int R>
+constexpr int nsv_of() { return R <= 16 ? 3 : 2; }
 constexpr int KST = kKeys * DH * 2;       // one K (or V) stage: 32 KB
 constexpr int KBLK = kKeys * 128;         // one 64-column block of a stage
 constexpr uint32_t kSCol = 0;             // TMEM: S^T buffers at columns 0 and 32
@@ -76,7 +80,7 @@ template <int R>
 constexpr size_t smem_bytes()
 {
     constexpr int NR = nr_of<R>();
-    return 1024 + (size_t)NSK * KST + (size_t)NSV * KST + 2 * NR * 128 /*Q*/ + 2 * 2 * NR * 128 /*P^T x2*/ +
+    return 1024 + (size_t)NSK * KST + (size_t)nsv_of<R>() * KST + 2 * NR * 128 /*Q*/ + 2 * 2 * NR * 128 /*P^T x2*/ +
            (size_t)R * kKeys * 4 /*p, fp32*/ + kSmallBytes;
 }
 
@@ -337,6 +341,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) dec_kernel(const __grid_cons
 {
     using namespace dec;
     constexpr int NR = nr_of<R>();
+    constexpr int NSV = nsv_of<R>();
     constexpr int PASSES = (R * 16 + 127) / 128;  // softmax passes over the row-sum chains
     constexpr int PPT = kKeys / 16;  // pages per tile
     constexpr int TPL = 16 / PPT;    // tiles whose block ids one 16-lane read covers
