@@ -1023,7 +1023,8 @@ bool plan_attention(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
 
 // Head dim 128 decode with the MMA operands swapped (pa_decode.cu).
 cudaError_t init_decode_attributes();
-int decode_rows(const AttnPlan &pl, int32_t max_query_len);
+int decode_rows(const AttnPlan &pl, int32_t max_query_len, int32_t num_seqs);
+long long decode_grid(const AttnPlan &pl, int32_t num_seqs, int32_t num_kv_heads, int num_sms);
 cudaError_t launch_decode(const AttnArgs &a, const AttnPlan &pl, AttnParams &p, int rows, cudaStream_t stream);
 
 template <int DH, bool PAIR, int KT = 128>
@@ -1127,7 +1128,7 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
     p.scale_log2 = a.scale * 1.4426950408889634f;
     if constexpr (DH == 128) {
         // few query rows per CTA: the decode kernel with swapped operands
-        if (const int nr = decode_rows(pl, a.max_query_len))
+        if (const int nr = decode_rows(pl, a.max_query_len, a.num_seqs))
             return launch_decode(a, pl, p, nr, stream);
     }
     cudaLaunchConfig_t cfg = {};
@@ -1161,13 +1162,16 @@ static cudaError_t launch_dh(const AttnArgs &a, const AttnPlan &pl, ErrState *er
 cudaError_t launch_attention(const AttnArgs &a, const AttnPlan &pl, ErrState *err, cudaStream_t stream,
                              char *info, size_t info_len)
 {
-    const int nr = decode_rows(pl, a.max_query_len);
+    const int nr = decode_rows(pl, a.max_query_len, a.num_seqs);
+    // the decode kernel deals the split-KV chunks out as one wave of ranges
+    const long long grid =
+        nr ? decode_grid(pl, a.num_seqs, a.num_kv_heads, num_sms_of_current_device()) : pl.grid;
     if (info && info_len)
         snprintf(info, info_len,
                  "attention dh=%d schedule=%s grid=%lld qtiles=%d chunks=%d kv_tile=%d chunk=%d cpu=%d kernel=%s",
                  pl.head_dim,
                  pl.split ? "split-kv" : (pl.head_dim == 512 ? "in-cta-pair" : (pl.cl == 2 ? "in-cta-pair2sm" : "in-cta")),
-                 pl.grid, pl.qtiles, pl.nch, pl.kt, pl.head_dim == 128 ? Cfg<128>::kChunk : 0, pl.cpu,
+                 grid, pl.qtiles, pl.nch, pl.kt, pl.head_dim == 128 ? Cfg<128>::kChunk : 0, nr ? 0 : pl.cpu,
                  nr ? "decode-swapped-r" : "rows-m128");
     if (nr && info && info_len) {
         const size_t used = strlen(info);

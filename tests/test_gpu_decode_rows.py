@@ -116,3 +116,78 @@ def test_single_cta_schedule_equals_split():
     o = out.float().cpu().double()[[0, 17, 79]]
     assert float((o - torch.from_numpy(ref_o)).abs().max()) <= OUT_ATOL
     assert lse_rel_err(lse.cpu().numpy()[[0, 17, 79]], ref_l) <= LSE_RTOL
+
+
+def _alone(dw, w, b):
+    """Request b of the batch launched on its own (its q row(s), table row,
+    length), sharing the batch's cache."""
+    dev = dw.q.device
+    q0, q1 = int(w.query_start_loc[b]), int(w.query_start_loc[b + 1])
+    o, l = dw.attention(q=dw.q[q0:q1].contiguous(), block_tables=dw.block_tables[b:b + 1].contiguous(),
+                        seq_lens=dw.seq_lens[b:b + 1].contiguous(),
+                        query_start_loc=torch.tensor([0, q1 - q0], dtype=torch.int32, device=dev),
+                        max_seq_len=int(w.seq_lens[b]), max_query_len=max(1, q1 - q0))
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    return o, l, q0, q1
+
+
+@pytest.mark.parametrize("hq,hkv,nreq,seed", [
+    (8, 2, 40, 7),     # G = 4, up to 2 query tokens: 8 rows
+    (8, 1, 151, 8),    # 151 groups: the largest split-KV batch, 16 rows
+    (16, 4, 30, 9),    # G = 4 with four KV heads per request
+])
+def test_balanced_ranges_match_oracle_and_single_requests(hq, hkv, nreq, seed):
+    """Split-KV deals the chunks of all (request, KV head) groups out as one
+    wave of equal contiguous ranges: ranges start and end inside groups, hold
+    several whole groups, and skip a request without query tokens.  Every row
+    against the oracle, and chosen requests bit for bit against the same
+    request launched alone (a different cut: whole groups folded in one CTA
+    against records folded by the last arrival)."""
+    import random
+    rnd = random.Random(seed)
+    lens = [rnd.choice([1, 100, 128, 129, 256, 257, 700, rnd.randint(1, 5000)]) for _ in range(nreq)]
+    qlens = [min(L, rnd.choice([1, 1, 1, 2])) for L in lens]
+    qlens[3] = 0
+    w = _suffix_batch(hq, hkv, lens, qlens, seed=seed)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    print(info)
+    assert "decode-swapped" in info and "split" in info
+    ref_o, ref_l = oracle_attention(w)
+    err_o = float((out.float().cpu().double() - torch.from_numpy(ref_o)).abs().max())
+    err_l = lse_rel_err(lse.cpu().numpy(), ref_l)
+    print(f"oracle: out max_abs_diff={err_o:.3e} lse rel={err_l:.3e}")
+    assert err_o <= OUT_ATOL and err_l <= LSE_RTOL
+    for b in sorted({0, 2, 4, nreq // 2, nreq - 1}):
+        if qlens[b] == 0:
+            continue
+        o1, l1, q0, q1 = _alone(dw, w, b)
+        _bitwise(out[q0:q1], o1, f"request {b} (L={lens[b]}) in the batch vs alone")
+        _bitwise(lse[q0:q1], l1, f"request {b} lse")
+
+
+def test_scaled_decode_mix_matches_single_requests():
+    """The decode length mix repeated 16 times (64 requests, 2432 chunks over
+    one wave of CTAs): sampled rows against the oracle, and requests of each
+    length bit for bit against the same request alone."""
+    lens = list(wl.DECODE_LENS) * 16
+    w = wl.decode(seq_lens=lens, num_blocks=sum(wl.pages_needed(L) for L in lens) + 64)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    print(info)
+    assert "decode-swapped-r4" in info and "split" in info
+    rows = [0, 1, 2, 3, 29, 30, 41, 63]
+    ref_o, ref_l = oracle_attention(w, rows=rows)
+    o = out.float().cpu().double()[rows]
+    assert float((o - torch.from_numpy(ref_o)).abs().max()) <= OUT_ATOL
+    assert lse_rel_err(lse.cpu().numpy()[rows], ref_l) <= LSE_RTOL
+    for b in (0, 1, 2, 3, 30, 63):
+        o1, l1, q0, q1 = _alone(dw, w, b)
+        _bitwise(out[q0:q1], o1, f"request {b} (L={lens[b]}) in the batch vs alone")
+        _bitwise(lse[q0:q1], l1, f"request {b} lse")
