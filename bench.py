@@ -322,6 +322,21 @@ def run_ours(args, ws, rank, local):
                                            "traffic": None, "peak_source": pf["peak_source"]}}),
                   flush=True)
         return
+    if args.workload == "decode_scaled":
+        ds = measure_decode_scaled(args, dev, stream, ws, peaks, peak_src, launches=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": ds["gbs"], "unit": "GB/s",
+                              "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
+                              "ms_per_step": ds["us_per_launch"] / 1e3, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                              "data": "synthetic", "config": {"workload": ds["workload"],
+                                                               "schedule": ds["schedule"]},
+                              "gpu_launches": args.steps,
+                              "roofline": {"bound": "hbm", "achieved": ds["gbs"], "peak": ds["peak"],
+                                           "unit": "GB/s", "frac": ds["frac"], "traffic": None,
+                                           "peak_source": ds["peak_source"]}}),
+                  flush=True)
+        return
     if args.workload == "gather":
         ga = measure_gather(args, dev, stream, ws, peaks, peak_src, launches=args.steps)
         if rank == 0:
@@ -855,9 +870,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill", "wide", "gather"], default="decode",
-                    help="decode (default, the headline), or one causal prefill alone: "
-                         "prefill (Dh=128, 4096) or wide (Dh=512, 18432)")
+    ap.add_argument("--workload", choices=["decode", "prefill", "wide", "gather", "decode_scaled"],
+                    default="decode",
+                    help="decode (default, the headline), one causal prefill alone: prefill (Dh=128, "
+                         "4096) or wide (Dh=512, 18432), the compact gather, or decode_scaled (the "
+                         "decode length mix x16, attention launches alone)")
     ap.add_argument("--replicas", type=int, default=16)
     ap.add_argument("--wide-len", type=int, default=18432,
                     help="sequence length of the Dh=512 prefill (3072, 8192, 11264 or 18432)")
