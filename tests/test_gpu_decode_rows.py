@@ -191,3 +191,79 @@ def test_scaled_decode_mix_matches_single_requests():
         o1, l1, q0, q1 = _alone(dw, w, b)
         _bitwise(out[q0:q1], o1, f"request {b} (L={lens[b]}) in the batch vs alone")
         _bitwise(lse[q0:q1], l1, f"request {b} lse")
+
+
+def _deal(lens, qlens, hkv, num_sms):
+    """The split-KV deal of the decode kernel, recomputed on the host: for
+    each (request, KV head) group, whether one CTA's range holds all of its
+    256-key chunks."""
+    nch = [(L + 255) // 256 if q > 0 else 0 for L, q in zip(lens, qlens)]
+    pre = [0]
+    for c in nch:
+        pre.append(pre[-1] + c)
+    T = hkv * pre[-1]
+    G = min(num_sms, T)
+    cta_of = lambda x: ((x + 1) * G + T - 1) // T - 1
+    whole = {}
+    for b, c in enumerate(nch):
+        for k in range(hkv):
+            if c:
+                gs = hkv * pre[b] + k * c
+                whole[(b, k)] = cta_of(gs) == cta_of(gs + c - 1)
+    return whole
+
+
+def test_bad_block_ids_in_whole_and_cut_groups():
+    """A block id out of range in a request whose groups one CTA folds alone,
+    and in one whose groups are cut between CTAs: PA_ERR_BAD_METADATA, NaN
+    rows for those two requests, every other row bit for bit unchanged."""
+    import random
+    rnd = random.Random(21)
+    lens = [rnd.choice([100, 300, 700, 1500, 2500]) for _ in range(40)]
+    qlens = [1] * 40
+    w = _suffix_batch(8, 2, lens, qlens, seed=21)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    assert "decode-swapped" in pagedattn.last_launch_info() and "split" in pagedattn.last_launch_info()
+    whole = _deal(lens, qlens, 2, torch.cuda.get_device_properties(0).multi_processor_count)
+    b_whole = next(b for b in range(40) if whole[(b, 0)] and whole[(b, 1)] and lens[b] > 16)
+    b_cut = next(b for b in range(40) if not whole[(b, 0)] and not whole[(b, 1)] and b != b_whole)
+    bt = dw.block_tables.clone()
+    bt[b_whole, (lens[b_whole] - 1) // 16] = w.num_blocks + 3      # its last page
+    bt[b_cut, 0] = -7                                                # its first page
+    o2, l2 = dw.attention(block_tables=bt)
+    st, idx = pagedattn.check_errors()
+    assert st == pagedattn.PA_ERR_BAD_METADATA and idx in (b_whole, b_cut)
+    for b in (b_whole, b_cut):
+        assert torch.isnan(o2[b].float()).all() and torch.isnan(l2[b]).all(), b
+    keep = [b for b in range(40) if b not in (b_whole, b_cut)]
+    _bitwise(out[keep], o2[keep], f"other requests (bad ids in {b_whole} whole, {b_cut} cut)")
+    _bitwise(lse[keep], l2[keep], "other requests lse")
+
+
+def test_long_sequences_many_chunks_per_cta():
+    """Requests up to 150,000 keys: ranges of about ten chunks per CTA, so the
+    bad-id flag ring and the Q double buffer wrap, groups span several CTAs
+    and short groups sit inside one range.  Every row against the oracle;
+    the longest request bit for bit against the same request alone."""
+    lens = [150000, 1000, 40000, 700]
+    qlens = [1, 1, 1, 1]
+    w = _suffix_batch(8, 2, lens, qlens, seed=33)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    print(info)
+    assert "decode-swapped-r4" in info and "split" in info
+    ref_o, ref_l = oracle_attention(w)
+    err_o = float((out.float().cpu().double() - torch.from_numpy(ref_o)).abs().max())
+    err_l = lse_rel_err(lse.cpu().numpy(), ref_l)
+    print(f"oracle: out max_abs_diff={err_o:.3e} lse rel={err_l:.3e}")
+    assert err_o <= OUT_ATOL and err_l <= LSE_RTOL
+    for b in (0, 2):
+        o1, l1, q0, q1 = _alone(dw, w, b)
+        _bitwise(out[q0:q1], o1, f"request {b} (L={lens[b]}) in the batch vs alone")
+        _bitwise(lse[q0:q1], l1, f"request {b} lse")
