@@ -1,7 +1,7 @@
-// Split-KV pieces shared by the attention kernels that split a request's
-// keys over several CTAs (pa_attn.cu, pa_decode.cu): the partial-state record
-// layout, the compacted unit schedule and the arrival + left-to-right fold of
-// the chunk states (C5, C6).
+// Split-KV pieces of the attention kernels that split a request's keys over
+// several CTAs: the partial-state record layout (pa_attn.cu and pa_decode.cu),
+// and for the 128-row kernel (pa_attn.cu) the compacted unit schedule and the
+// arrival + left-to-right fold of the chunk states (C5, C6).
 #pragma once
 #include "pa_attn_common.cuh"
 
