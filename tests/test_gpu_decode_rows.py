@@ -267,3 +267,39 @@ def test_long_sequences_many_chunks_per_cta():
         o1, l1, q0, q1 = _alone(dw, w, b)
         _bitwise(out[q0:q1], o1, f"request {b} (L={lens[b]}) in the batch vs alone")
         _bitwise(lse[q0:q1], l1, f"request {b} lse")
+
+
+@pytest.mark.parametrize("nreq,hkv,qmax,split", [
+    (80, 2, 8, False),   # 160 groups: one CTA per group, 32 rows
+    (76, 2, 4, False),   # 152 groups: one CTA per group, 16 rows
+    (30, 2, 8, True),    # 32 rows, ranges of several chunks across groups
+    (50, 2, 3, True),    # 16 rows (G x 3 tokens), ranges across groups
+])
+def test_speculative_rows_both_schedules(nreq, hkv, qmax, split):
+    """Several query tokens per request (up to 32 rows per group) on both
+    schedules: every row against the oracle, and chosen requests bit for bit
+    against the same request alone."""
+    import random
+    rnd = random.Random(nreq * 7 + qmax)
+    lens = [rnd.randint(600, 3500) for _ in range(nreq)]
+    qlens = [rnd.randint(1, qmax) for _ in range(nreq)]
+    qlens[0] = qmax
+    w = _suffix_batch(8, hkv, lens, qlens, seed=nreq + qmax)
+    dw = DeviceWorkload(w)
+    dw.write_cache()
+    out, lse = dw.attention()
+    assert pagedattn.check_errors() == (pagedattn.PA_OK, -1)
+    info = pagedattn.last_launch_info()
+    print(info)
+    rows = 4 * qmax
+    expect = next(r for r in (4, 8, 16, 32) if rows <= r)
+    assert f"decode-swapped-r{expect}" in info and (("split" in info) == split), info
+    ref_o, ref_l = oracle_attention(w)
+    err_o = float((out.float().cpu().double() - torch.from_numpy(ref_o)).abs().max())
+    err_l = lse_rel_err(lse.cpu().numpy(), ref_l)
+    print(f"oracle: out max_abs_diff={err_o:.3e} lse rel={err_l:.3e}")
+    assert err_o <= OUT_ATOL and err_l <= LSE_RTOL
+    for b in (0, 1, nreq // 2, nreq - 1):
+        o1, l1, q0, q1 = _alone(dw, w, b)
+        _bitwise(out[q0:q1], o1, f"request {b} (L={lens[b]}, q={qlens[b]}) in the batch vs alone")
+        _bitwise(lse[q0:q1], l1, f"request {b} lse")
