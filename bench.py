@@ -616,14 +616,17 @@ def _packed(tensors, device=None, pin=False):
 
 
 def measure_e2e(args, w, reps, dev, kv_bytes, ws):
-    """Same metric through the public API with host buffers: each step copies
+    """Same metric through the public API with host buffers: each step moves
     its inputs (new K/V tokens, slots, q, tables, lengths) from pinned host
-    memory in one transfer, issues the composed cache-write + attention call
-    (prepared once: validated and marshalled outside the loop) and copies
-    out + lse back to pinned host memory in one transfer.  Two issue modes,
-    both wall clock: the steps recorded once into CUDA graphs and replayed
-    (how a serving loop issues a fixed-shape step; reported as the value),
-    and each step issued from Python (reported beside it)."""
+    memory to the device, issues the composed cache-write + attention call
+    (prepared once: validated and marshalled outside the loop) and brings
+    out + lse back to pinned host memory.  The value: the inputs copied by
+    the library's staging kernel (pa_copy_to_device reads the pinned buffer
+    over the CPU-GPU link), the results written by the attention kernels
+    straight into the pinned host buffer.  Beside it, the same step with one
+    copy-engine transfer each way (torch copies).  Both wall clock, the steps
+    recorded once into CUDA graphs and replayed (how a serving loop issues a
+    fixed-shape step); each step issued from Python is reported too."""
     from paged_kv_cache_178_gb300 import pagedattn
     last = last_token_rows(w)
     host_src = (w.key[last].contiguous(), w.value[last].contiguous(), w.slot_mapping[last].contiguous(),
@@ -633,12 +636,16 @@ def measure_e2e(args, w, reps, dev, kv_bytes, ws):
     for v, t in zip(h_views, host_src):
         v.copy_(t)
     res_shape = (torch.empty(w.q.shape, dtype=torch.bfloat16), torch.empty(w.q.shape[:2], dtype=torch.float32))
-    h_res, _ = _packed(res_shape, pin=True)
+    h_res, (h_out, h_lse) = _packed(res_shape, pin=True)
     stream = torch.cuda.Stream(device=dev)
-    calls, calls2, d_ins, d_ress = [], [], [], []
+    staged, calls, calls2, d_ins, d_ress = [], [], [], [], []
     for dw in reps:
         d_in, (k, v, s, q, bt, sl, qsl) = _packed(host_src, device=dev)
         d_res, (out, lse) = _packed(res_shape, device=dev)
+        staged.append((pagedattn.prepare_copy_to_device(d_in, h_in, stream=stream),
+                       pagedattn.prepare_reshape_and_paged_attention(
+                           k, v, s, q, dw.k_cache, dw.v_cache, bt, sl, qsl, w.scale, w.max_query_len,
+                           w.max_seq_len, h_out, h_lse, dw.workspace, stream=stream)))
         calls.append(pagedattn.prepare_reshape_and_paged_attention(
             k, v, s, q, dw.k_cache, dw.v_cache, bt, sl, qsl, w.scale, w.max_query_len, w.max_seq_len, out,
             lse, dw.workspace, stream=stream))
@@ -653,6 +660,12 @@ def measure_e2e(args, w, reps, dev, kv_bytes, ws):
     bytes_out = sum(t.numel() * t.element_size() for t in res_shape)
 
     def step(i):
+        r = i % R
+        stage, call = staged[r]
+        stage()
+        call()
+
+    def step_copy_engine(i):
         r = i % R
         d_ins[r].copy_(h_in, non_blocking=True)
         calls[r]()
@@ -681,28 +694,33 @@ def measure_e2e(args, w, reps, dev, kv_bytes, ws):
             for i in range(n):
                 step(i)
 
+    def graphed_time(fn, n):
+        g = GraphedSteps(fn, R, stream, chunk=200)
+        g.prepare(n)
+        g.run(max(args.warmup, 3))
+        return wall(g.run, n)
+
     n = min(args.steps, 2000)
     eager(max(args.warmup, 3))
     t_eager = wall(eager, n)
-    graphed = GraphedSteps(step, R, stream, chunk=200)
-    graphed.prepare(n)
-    graphed.run(max(args.warmup, 3))
-    t_graph = wall(graphed.run, n)
-    graphed2 = GraphedSteps(step_two_calls, R, stream, chunk=200)
-    graphed2.prepare(n)
-    graphed2.run(max(args.warmup, 3))
-    t_graph2 = wall(graphed2.run, n)
+    t_graph = graphed_time(step, n)
+    t_graph_ce = graphed_time(step_copy_engine, n)
+    t_graph2 = graphed_time(step_two_calls, n)
     value = aggregate_value(kv_bytes * n / 1e9, t_graph, ws, dev)
     value_eager = aggregate_value(kv_bytes * n / 1e9, t_eager, ws, dev)
+    value_ce = aggregate_value(kv_bytes * n / 1e9, t_graph_ce, ws, dev)
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": bytes_in,
             "d2h_bytes_per_step": bytes_out, "steps": n,
             "ms_per_step": round(t_graph / n * 1e3, 4),
             "eager_value": round(value_eager, 2), "eager_ms_per_step": round(t_eager / n * 1e3, 4),
+            "copy_engine_value": round(value_ce, 2), "copy_engine_ms_per_step": round(t_graph_ce / n * 1e3, 4),
             "two_calls_ms_per_step": round(t_graph2 / n * 1e3, 4),
-            "how": "public API call prepared once; per step one pinned host-to-device copy, the call and "
-                   "one device-to-host copy; steps replayed from CUDA graphs of 200, wall clock "
-                   "(eager_*: the same steps issued one by one from Python; two_calls_*: graph replay "
-                   "of the step as pa_reshape_and_cache + pa_paged_attention)"}
+            "how": "public API calls prepared once; per step pa_copy_to_device (the staging kernel reads the "
+                   "step's packed inputs from pinned host memory) and the composed call, whose attention "
+                   "writes out and lse into pinned host memory; steps replayed from CUDA graphs of 200, wall "
+                   "clock (eager_*: the same steps issued one by one from Python; copy_engine_*: one torch "
+                   "host-to-device and one device-to-host copy around the composed call instead; "
+                   "two_calls_*: that, with the step as pa_reshape_and_cache + pa_paged_attention)"}
 
 
 # ---------------------------------------------------- CPU oracle (baseline) --

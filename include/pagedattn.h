@@ -157,6 +157,9 @@ PA_API size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_
  *   out               : [num_q_tokens, Hq, Dh] BF16, contiguous.  Rows of
  *                       tokens owned by no request are left untouched.
  *   lse               : [num_q_tokens, Hq] fp32, contiguous, or NULL.
+ *                       out and lse may be device memory or page-locked host
+ *                       memory mapped into the device's address space (the
+ *                       kernels write them with plain stores).
  *   block_tables      : [num_seqs, max_blocks_per_seq] int32.
  *   seq_lens          : [num_seqs] int32.  query_start_loc: [num_seqs+1] int32,
  *                       non-decreasing, last entry <= num_q_tokens.
@@ -189,6 +192,26 @@ PA_API pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t
                              int32_t num_seqs, int32_t max_query_len, int32_t max_seq_len,
                              float scale, void *out, float *lse, void *workspace,
                              size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Copies `bytes` bytes from `src` to device memory `dst` with a kernel on
+ * `stream`, for step inputs that arrive in host memory.  `src` is page-locked
+ * host memory mapped into the device's address space (cudaHostAlloc, or
+ * cudaHostRegister with cudaHostRegisterMapped) or device memory; the kernel
+ * reads it directly (on a coherent CPU-GPU link, one round trip instead of a
+ * copy-engine transfer).
+ *   - The paper (the source pages) has no counterpart to this entry point.
+ *   - Launched with programmatic stream serialization: it waits for the
+ *     preceding grid of the stream to complete before it reads or writes, and
+ *     lets the next kernel of the stream (for instance the cache write of
+ *     pa_reshape_and_paged_attention, which waits for it in turn) be
+ *     scheduled meanwhile.
+ *   - dst and src 16-byte aligned, not overlapping; otherwise
+ *     PA_ERR_INVALID_ARG and nothing is launched.  bytes == 0 launches nothing.
+ * The attention calls may likewise be given `out` and `lse` in page-locked,
+ * mapped host memory: their kernels write the results there directly.
+ */
+PA_API pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, pa_stream_t stream);
 
 /*
  * PagedAttention for callers that cannot allocate device memory.

@@ -112,6 +112,34 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     }
 }
 
+// Staging copy (pa_copy_to_device): 16-byte vectors, up to four per thread
+// per pass with every load issued before the stores, so a source in host
+// memory costs one round trip over the CPU-GPU link per pass; the bytes past
+// the last whole vector go one by one.
+__global__ void __launch_bounds__(256) copy_to_device_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
+                                                             int64_t n16, uint8_t *__restrict__ dst_tail,
+                                                             const uint8_t *__restrict__ src_tail, int tail)
+{
+    // programmatic stream serialization: the preceding grid may still read
+    // dst or write src until it has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < n16; base += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (base + i * stride < n16)
+                v[i] = src[base + i * stride];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (base + i * stride < n16)
+                dst[base + i * stride] = v[i];
+    }
+    if (blockIdx.x == 0 && (int)threadIdx.x < tail)
+        dst_tail[threadIdx.x] = src_tail[threadIdx.x];
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -352,6 +380,46 @@ pa_status pa_reshape_and_cache(const void *key, int64_t key_tok_stride, const vo
     if (num_tokens > 0 && (st = device_setup(&err)) != PA_OK)
         return st;
     return reshape_launch(c, err, reinterpret_cast<cudaStream_t>(stream), g_last_info, sizeof g_last_info);
+}
+
+pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, pa_stream_t stream)
+{
+    if (bytes == 0)
+        return PA_OK;
+    if (!dst || !src)
+        return PA_ERR_INVALID_ARG;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + bytes && s < d + bytes)
+        return PA_ERR_INVALID_ARG;  // overlapping ranges
+    if ((d | s) & 15u)
+        return PA_ERR_INVALID_ARG;  // both 16-byte aligned
+    ErrState *err = nullptr;
+    pa_status st = device_setup(&err);
+    if (st != PA_OK)
+        return st;
+    const int64_t n16 = (int64_t)(bytes / 16);
+    const int tail = (int)(bytes % 16);
+    int64_t blocks = (n16 + 4 * 256 - 1) / (4 * 256);
+    if (blocks < 1)
+        blocks = 1;
+    if (blocks > 152 * 8)
+        blocks = 152 * 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, copy_to_device_kernel, static_cast<uint4 *>(dst), static_cast<const uint4 *>(src),
+                           n16, static_cast<uint8_t *>(dst) + n16 * 16, static_cast<const uint8_t *>(src) + n16 * 16,
+                           tail);
+    snprintf(g_last_info, sizeof g_last_info, "copy_to_device bytes=%zu grid=%lld block=256", bytes,
+             (long long)blocks);
+    return cuda_status(e);
 }
 
 size_t pa_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

@@ -38,7 +38,7 @@ PA_ERR_CUDA = 6
 EXPORTED = ("pa_init", "pa_reshape_and_cache", "pa_paged_attention_workspace_size",
             "pa_paged_attention", "pa_paged_attention_noalloc", "pa_reshape_and_paged_attention",
             "pa_gather_kv_head", "pa_check_errors", "pa_set_fold_wait_limit_ns",
-            "pa_status_string", "pa_last_launch_info")
+            "pa_copy_to_device", "pa_status_string", "pa_last_launch_info")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -94,6 +94,8 @@ def load(path: str = LIB_PATH):
         lib.pa_check_errors.argtypes = [vp, ctypes.POINTER(i64)]
         lib.pa_set_fold_wait_limit_ns.restype = ctypes.c_uint64
         lib.pa_set_fold_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.pa_copy_to_device.restype = i32
+        lib.pa_copy_to_device.argtypes = [vp, vp, sz, vp]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_status_string.argtypes = [i32]
         lib.pa_last_launch_info.restype = None
@@ -226,6 +228,9 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
         lse = torch.empty((tq, hq), dtype=torch.float32, device=q.device)
     if lse is not None and (lse.shape != (tq, hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous [Tq, Hq] fp32 tensor")
+    _check_result_tensor("out", out)
+    if lse is not None:
+        _check_result_tensor("lse", lse)
     need = workspace_size(num_seqs, hq, c.num_kv_heads, dh, max_query_len, max_seq_len)
     if workspace is None and need > 0:
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
@@ -274,6 +279,35 @@ class PreparedCall:
             raise PagedAttnError(st, self._what)
 
 
+def _check_result_tensor(name: str, t: torch.Tensor) -> None:
+    """out / lse: device memory, or page-locked host memory the kernels write
+    directly (mapped into the device's address space)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+
+
+def prepare_copy_to_device(dst: torch.Tensor, src: torch.Tensor,
+                           stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """pa_copy_to_device of all of src's bytes into dst (a CUDA tensor of the
+    same byte size; src a pinned host tensor or a CUDA tensor), validated now
+    and issued by each call of the result."""
+    nbytes = src.numel() * src.element_size()
+    if not dst.is_cuda or not dst.is_contiguous() or not src.is_contiguous() \
+            or dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst must be a contiguous CUDA tensor of src's byte size")
+    if not (src.is_cuda or src.is_pinned()):
+        raise ValueError("src must be a pinned host tensor or a CUDA tensor")
+    lib = load()
+    return PreparedCall(lib.pa_copy_to_device, (dst.data_ptr(), src.data_ptr(), nbytes, _stream_handle(stream)),
+                        "pa_copy_to_device", (dst, src))
+
+
+def copy_to_device(dst: torch.Tensor, src: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy src (pinned host or CUDA) into the CUDA tensor dst with the
+    library's staging kernel."""
+    prepare_copy_to_device(dst, src, stream)()
+
+
 def prepare_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
                               v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                               stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
@@ -301,6 +335,9 @@ def prepare_paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         raise ValueError("out must be a contiguous [Tq, Hq, Dh] BF16 tensor")
     if lse is not None and (lse.shape != (tq, hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous [Tq, Hq] fp32 tensor")
+    _check_result_tensor("out", out)
+    if lse is not None:
+        _check_result_tensor("lse", lse)
     need = workspace_size(num_seqs, hq, c.num_kv_heads, dh, max_query_len, max_seq_len)
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if ws_len < need:
@@ -324,6 +361,9 @@ def _composition_args(key, value, slot_mapping, q, k_cache, v_cache, block_table
         raise ValueError("out must be a contiguous [Tq, Hq, Dh] BF16 tensor")
     if lse is not None and (lse.shape != (tq, hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous [Tq, Hq] fp32 tensor")
+    _check_result_tensor("out", out)
+    if lse is not None:
+        _check_result_tensor("lse", lse)
     need = workspace_size(num_seqs, hq, c.num_kv_heads, dh, max_query_len, max_seq_len)
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if ws_len < need:
