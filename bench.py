@@ -642,7 +642,7 @@ def measure_e2e(args, w, reps, dev, kv_bytes, ws):
     for dw in reps:
         d_in, (k, v, s, q, bt, sl, qsl) = _packed(host_src, device=dev)
         d_res, (out, lse) = _packed(res_shape, device=dev)
-        staged.append((pagedattn.prepare_copy_to_device(d_in, h_in, stream=stream),
+        staged.append((pagedattn.prepare_copy_to_device(d_in, h_in, stream=stream, src_ready=True),
                        pagedattn.prepare_reshape_and_paged_attention(
                            k, v, s, q, dw.k_cache, dw.v_cache, bt, sl, qsl, w.scale, w.max_query_len,
                            w.max_seq_len, h_out, h_lse, dw.workspace, stream=stream)))
@@ -716,7 +716,8 @@ def measure_e2e(args, w, reps, dev, kv_bytes, ws):
             "copy_engine_value": round(value_ce, 2), "copy_engine_ms_per_step": round(t_graph_ce / n * 1e3, 4),
             "two_calls_ms_per_step": round(t_graph2 / n * 1e3, 4),
             "how": "public API calls prepared once; per step pa_copy_to_device (the staging kernel reads the "
-                   "step's packed inputs from pinned host memory) and the composed call, whose attention "
+                   "step's packed inputs from pinned host memory, which only the host writes: src_ready) and "
+                   "the composed call, whose attention "
                    "writes out and lse into pinned host memory; steps replayed from CUDA graphs of 200, wall "
                    "clock (eager_*: the same steps issued one by one from Python; copy_engine_*: one torch "
                    "host-to-device and one device-to-host copy around the composed call instead; "

@@ -202,16 +202,21 @@ PA_API pa_status pa_paged_attention(const void *q, int64_t num_q_tokens, int64_t
  * copy-engine transfer).
  *   - The paper (the source pages) has no counterpart to this entry point.
  *   - Launched with programmatic stream serialization: it waits for the
- *     preceding grid of the stream to complete before it reads or writes, and
- *     lets the next kernel of the stream (for instance the cache write of
- *     pa_reshape_and_paged_attention, which waits for it in turn) be
- *     scheduled meanwhile.
+ *     preceding grid of the stream to complete before it writes dst (and,
+ *     unless src_ready, before it reads src), and lets the next kernel of the
+ *     stream (for instance the cache write of pa_reshape_and_paged_attention,
+ *     which waits for it in turn) be scheduled meanwhile.
+ *   - src_ready != 0 is the caller's statement that no kernel in flight on
+ *     the GPU writes src (for instance host memory filled by the host before
+ *     the call): the kernel then reads src at once, while the preceding grid
+ *     may still run.
  *   - dst and src 16-byte aligned, not overlapping; otherwise
  *     PA_ERR_INVALID_ARG and nothing is launched.  bytes == 0 launches nothing.
  * The attention calls may likewise be given `out` and `lse` in page-locked,
  * mapped host memory: their kernels write the results there directly.
  */
-PA_API pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, pa_stream_t stream);
+PA_API pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, int32_t src_ready,
+                                   pa_stream_t stream);
 
 /*
  * PagedAttention for callers that cannot allocate device memory.

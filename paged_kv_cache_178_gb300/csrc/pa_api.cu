@@ -115,29 +115,45 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
 // Staging copy (pa_copy_to_device): 16-byte vectors, up to four per thread
 // per pass with every load issued before the stores, so a source in host
 // memory costs one round trip over the CPU-GPU link per pass; the bytes past
-// the last whole vector go one by one.
+// the last whole vector go one by one.  With src_ready the first pass reads
+// before the wait for the preceding grid (no grid in flight writes src);
+// every store still waits for it (it may read dst).
 __global__ void __launch_bounds__(256) copy_to_device_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
                                                              int64_t n16, uint8_t *__restrict__ dst_tail,
-                                                             const uint8_t *__restrict__ src_tail, int tail)
+                                                             const uint8_t *__restrict__ src_tail, int tail,
+                                                             int src_ready)
 {
-    // programmatic stream serialization: the preceding grid may still read
-    // dst or write src until it has completed
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < n16; base += 4 * stride) {
-        uint4 v[4];
+    int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint4 v[4];
+    uint8_t t8 = 0;
+    const bool tail_thread = blockIdx.x == 0 && (int)threadIdx.x < tail;
+    if (src_ready) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (base + i * stride < n16)
                 v[i] = src[base + i * stride];
+        if (tail_thread)
+            t8 = src_tail[threadIdx.x];
+    }
+    // programmatic stream serialization: the preceding grid may still read
+    // dst (and, without src_ready, write src) until it has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (bool first = true; base < n16; base += 4 * stride, first = false) {
+        if (!first || !src_ready) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (base + i * stride < n16)
+                    v[i] = src[base + i * stride];
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (base + i * stride < n16)
                 dst[base + i * stride] = v[i];
     }
-    if (blockIdx.x == 0 && (int)threadIdx.x < tail)
-        dst_tail[threadIdx.x] = src_tail[threadIdx.x];
+    if (tail_thread)
+        dst_tail[threadIdx.x] = src_ready ? t8 : src_tail[threadIdx.x];
 }
 
 }  // namespace pa
@@ -382,7 +398,7 @@ pa_status pa_reshape_and_cache(const void *key, int64_t key_tok_stride, const vo
     return reshape_launch(c, err, reinterpret_cast<cudaStream_t>(stream), g_last_info, sizeof g_last_info);
 }
 
-pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, pa_stream_t stream)
+pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, int32_t src_ready, pa_stream_t stream)
 {
     if (bytes == 0)
         return PA_OK;
@@ -416,7 +432,7 @@ pa_status pa_copy_to_device(void *dst, const void *src, size_t bytes, pa_stream_
     const cudaError_t e =
         cudaLaunchKernelEx(&cfg, copy_to_device_kernel, static_cast<uint4 *>(dst), static_cast<const uint4 *>(src),
                            n16, static_cast<uint8_t *>(dst) + n16 * 16, static_cast<const uint8_t *>(src) + n16 * 16,
-                           tail);
+                           tail, src_ready ? 1 : 0);
     snprintf(g_last_info, sizeof g_last_info, "copy_to_device bytes=%zu grid=%lld block=256", bytes,
              (long long)blocks);
     return cuda_status(e);

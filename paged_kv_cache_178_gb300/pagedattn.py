@@ -95,7 +95,7 @@ def load(path: str = LIB_PATH):
         lib.pa_set_fold_wait_limit_ns.restype = ctypes.c_uint64
         lib.pa_set_fold_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.pa_copy_to_device.restype = i32
-        lib.pa_copy_to_device.argtypes = [vp, vp, sz, vp]
+        lib.pa_copy_to_device.argtypes = [vp, vp, sz, i32, vp]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_status_string.argtypes = [i32]
         lib.pa_last_launch_info.restype = None
@@ -287,10 +287,11 @@ def _check_result_tensor(name: str, t: torch.Tensor) -> None:
 
 
 def prepare_copy_to_device(dst: torch.Tensor, src: torch.Tensor,
-                           stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+                           stream: Optional[torch.cuda.Stream] = None, src_ready: bool = False) -> PreparedCall:
     """pa_copy_to_device of all of src's bytes into dst (a CUDA tensor of the
     same byte size; src a pinned host tensor or a CUDA tensor), validated now
-    and issued by each call of the result."""
+    and issued by each call of the result.  src_ready: no kernel in flight
+    writes src (e.g. host memory the host fills), so it is read at once."""
     nbytes = src.numel() * src.element_size()
     if not dst.is_cuda or not dst.is_contiguous() or not src.is_contiguous() \
             or dst.numel() * dst.element_size() != nbytes:
@@ -298,14 +299,16 @@ def prepare_copy_to_device(dst: torch.Tensor, src: torch.Tensor,
     if not (src.is_cuda or src.is_pinned()):
         raise ValueError("src must be a pinned host tensor or a CUDA tensor")
     lib = load()
-    return PreparedCall(lib.pa_copy_to_device, (dst.data_ptr(), src.data_ptr(), nbytes, _stream_handle(stream)),
+    return PreparedCall(lib.pa_copy_to_device,
+                        (dst.data_ptr(), src.data_ptr(), nbytes, 1 if src_ready else 0, _stream_handle(stream)),
                         "pa_copy_to_device", (dst, src))
 
 
-def copy_to_device(dst: torch.Tensor, src: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+def copy_to_device(dst: torch.Tensor, src: torch.Tensor, stream: Optional[torch.cuda.Stream] = None,
+                   src_ready: bool = False) -> None:
     """Copy src (pinned host or CUDA) into the CUDA tensor dst with the
     library's staging kernel."""
-    prepare_copy_to_device(dst, src, stream)()
+    prepare_copy_to_device(dst, src, stream, src_ready)()
 
 
 def prepare_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,

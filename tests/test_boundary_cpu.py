@@ -237,10 +237,10 @@ def test_noalloc_validates_before_any_cuda_call(lib):
 
 def test_copy_to_device_validates_before_any_cuda_call(lib):
     ok, bad = pagedattn.PA_OK, pagedattn.PA_ERR_INVALID_ARG
-    assert lib.pa_copy_to_device(FAKE, FAKE + 4096, 0, None) == ok          # nothing to copy
-    assert lib.pa_copy_to_device(None, FAKE, 64, None) == bad
-    assert lib.pa_copy_to_device(FAKE, None, 64, None) == bad
-    assert lib.pa_copy_to_device(FAKE, FAKE + 32, 64, None) == bad          # overlapping ranges
-    assert lib.pa_copy_to_device(FAKE + 32, FAKE, 64, None) == bad
-    assert lib.pa_copy_to_device(FAKE + 8, FAKE + 4096, 64, None) == bad    # dst not 16-byte aligned
-    assert lib.pa_copy_to_device(FAKE, FAKE + 4100, 64, None) == bad        # src not 16-byte aligned
+    assert lib.pa_copy_to_device(FAKE, FAKE + 4096, 0, 0, None) == ok          # nothing to copy
+    assert lib.pa_copy_to_device(None, FAKE, 64, 0, None) == bad
+    assert lib.pa_copy_to_device(FAKE, None, 64, 0, None) == bad
+    assert lib.pa_copy_to_device(FAKE, FAKE + 32, 64, 0, None) == bad          # overlapping ranges
+    assert lib.pa_copy_to_device(FAKE + 32, FAKE, 64, 0, None) == bad
+    assert lib.pa_copy_to_device(FAKE + 8, FAKE + 4096, 64, 0, None) == bad    # dst not 16-byte aligned
+    assert lib.pa_copy_to_device(FAKE, FAKE + 4100, 64, 0, None) == bad        # src not 16-byte aligned

@@ -12,12 +12,13 @@ from paged_kv_cache_178_gb300.device import DeviceWorkload
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("src_ready", [False, True])
 @pytest.mark.parametrize("nbytes", [16, 1000, 19524, 1 << 20, (1 << 20) + 7])
-def test_copy_to_device_exact_bytes(nbytes):
+def test_copy_to_device_exact_bytes(nbytes, src_ready):
     gen = torch.Generator().manual_seed(nbytes)
     src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=gen).pin_memory()
     dst = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda")
-    pagedattn.copy_to_device(dst, src)
+    pagedattn.copy_to_device(dst, src, src_ready=src_ready)
     torch.cuda.synchronize()
     assert torch.equal(dst.cpu(), src)
     # device to device as well
@@ -48,7 +49,7 @@ def test_host_staged_composed_call_equals_device_call():
     h = [t.pin_memory() for t in host]
     d = [torch.empty_like(t, device="cuda") for t in host]
     for dt, ht in zip(d, h):
-        pagedattn.copy_to_device(dt, ht)
+        pagedattn.copy_to_device(dt, ht, src_ready=True)   # only the host writes h
     k, v, s, q, bt, sl, qsl = d
     h_out = torch.full(w.q.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.full(w.q.shape[:2], float("nan"), dtype=torch.float32).pin_memory()
