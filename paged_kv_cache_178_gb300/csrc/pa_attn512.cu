@@ -30,8 +30,10 @@ constexpr int kHalfCols = 256;          // head-dim columns per CTA of the pair
 constexpr int kNKB = kHalfCols / 64;    // 64-column blocks per half
 constexpr int kTileBytes = kNKB * kKeys * 128;  // one KV half tile (32 KB)
 constexpr int kStagesK = 2, kStagesV = 2;
-constexpr int kXStride = 68;            // floats per exchanged row (64 + 4 pad: conflict-free)
-constexpr int kXBytes = kRows * kXStride * 4;
+// Partial-score exchange buffer of one S buffer: [2 halves][8 blocks of 4
+// columns][128 rows] of float4, so the 16-byte stores of a warp's 32 rows
+// into the peer (and their loads here) cover 512 contiguous bytes
+constexpr int kXBytes = 2 * 8 * kRows * 16;
 constexpr int kSmallBytes = 512 + 64 + 2 * 2 * kRows * 4 + kRows * 2 * 4;
 constexpr uint32_t kQCol = 0;           // TMEM: Q half (128 columns of BF16 pairs)
 constexpr uint32_t kSCol = 128;         // TMEM: two S/P buffers of 64 columns
@@ -64,7 +66,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sK = smem;
     uint8_t *sV = sK + NSK * kTileBytes;
-    float *sX = reinterpret_cast<float *>(sV + NSV * kTileBytes);   // [2][128][kXStride]
+    float4 *sX = reinterpret_cast<float4 *>(sV + NSV * kTileBytes);  // [2 S buffers][2 halves][8][128]
     uint8_t *small = reinterpret_cast<uint8_t *>(sX) + 2 * kXBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(small);
     int *sflags = reinterpret_cast<int *>(small + 512);  // [0] abort [1] tmem [3] bad
@@ -128,8 +130,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_PF + i), 8);
             mbar_init(bar(B_PV + i), 1);
-            mbar_init(bar(B_XF + i), 256);  // the peer's 256 softmax threads wrote their rows
-            mbar_init(bar(B_XE + i), 256);  // the peer's 256 softmax threads read what we wrote
+            mbar_init(bar(B_XF + i), 1);  // the peer's softmax threads have written their rows
+            mbar_init(bar(B_XE + i), 1);  // the peer's softmax threads have read what we wrote
         }
         mbar_init(bar(B_FIN), 8);
         mbar_init(bar(B_PROD), 1);
@@ -315,26 +317,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             if (okw) {
                 tmem_ld32(scol, v);
                 tmem_wait_ld();
-                const uint32_t dst = mapa_shared(smem_addr(sX + (sb * kRows + r) * kXStride + 32 * h), peer);
+                const uint32_t dst = mapa_shared(smem_addr(sX + ((sb * 2 + h) * 8) * kRows + r), peer);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    st_cluster_v4(dst + 16 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                mbar_arrive_cluster(mapa_shared(bar(B_XF + sb), peer));
-                okw = wbc(B_XF + sb, (it >> 1) & 1);
+                    st_cluster_v4(dst + i * kRows * 16, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
-            okw = __all_sync(0xffffffffu, okw);
+            // every softmax thread's rows are written: one release (cumulative
+            // over the barrier) and one arrival on the peer's barrier
+            if (named_sync_or(1, 256, !okw)) {
+                failed = true;
+                break;
+            }
+            if (tid == 128) {
+                fence_acq_rel_cluster();
+                mbar_arrive_cluster_relaxed(mapa_shared(bar(B_XF + sb), peer));
+            }
+            okw = __all_sync(0xffffffffu, wbc(B_XF + sb, (it >> 1) & 1));
             float s[32];
             if (okw) {
-                const float4 *src = reinterpret_cast<const float4 *>(sX + (sb * kRows + r) * kXStride + 32 * h);
+                const float4 *src = sX + ((sb * 2 + h) * 8) * kRows + r;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float4 x = src[i];
+                    const float4 x = src[i * kRows];
                     s[4 * i + 0] = __fadd_rn(__uint_as_float(v[4 * i + 0]), x.x);
                     s[4 * i + 1] = __fadd_rn(__uint_as_float(v[4 * i + 1]), x.y);
                     s[4 * i + 2] = __fadd_rn(__uint_as_float(v[4 * i + 2]), x.z);
                     s[4 * i + 3] = __fadd_rn(__uint_as_float(v[4 * i + 3]), x.w);
                 }
-                mbar_arrive_cluster(mapa_shared(bar(B_XE + sb), peer));  // our buffer sb is free again
             }
             const int nallow = row_valid ? max(0, min(32, pos - it * kKeys - 32 * h + 1)) : 0;
             float pmax = -INFINITY;
@@ -347,6 +356,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             if (named_sync_or(1, 256, !okw)) {
                 failed = true;
                 break;
+            }
+            if (tid == 128) {
+                // every softmax thread has read the peer's rows: our buffer sb is
+                // free again (one release and one arrival for all of them)
+                fence_acq_rel_cluster();
+                mbar_arrive_cluster_relaxed(mapa_shared(bar(B_XE + sb), peer));
             }
             const float tmax = __fmul_rn(fmaxf(xmax[r], xmax[kRows + r]), p.scale_log2);
             float m_new = m, corr = 1.f;

@@ -304,6 +304,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 // thread's memory writes (relaxed).  For hand-offs of tensor memory, whose
 // order is given by tcgen05.wait + tcgen05.fence::before_thread_sync, and of
 // pure counts.
+// Release fence at cluster scope: this thread's earlier memory operations,
+// and those ordered before it by a barrier, before its later ones.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
