@@ -130,7 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_PF + i), 8);
             mbar_init(bar(B_PV + i), 1);
-            mbar_init(bar(B_XF + i), 1);  // the peer's softmax threads have written their rows
+            mbar_init(bar(B_XF + i), 1);  // armed here each tile; the peer's rows land as its bytes
             mbar_init(bar(B_XE + i), 1);  // the peer's softmax threads have read what we wrote
         }
         mbar_init(bar(B_FIN), 8);
@@ -315,24 +315,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             const uint32_t scol = tmem + lane_off + kSCol + sb * kKeys + 32 * h;
             uint32_t v[32];
             if (okw) {
+                // this tile's incoming rows: 32 KB from the peer's st.async
+                if (tid == 128)
+                    mbar_arrive_expect_tx(bar(B_XF + sb), kXBytes);
                 tmem_ld32(scol, v);
                 tmem_wait_ld();
                 const uint32_t dst = mapa_shared(smem_addr(sX + ((sb * 2 + h) * 8) * kRows + r), peer);
+                const uint32_t rbar = mapa_shared(bar(B_XF + sb), peer);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    st_cluster_v4(dst + i * kRows * 16, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    st_async_v4(dst + i * kRows * 16, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], rbar);
+                okw = wbc(B_XF + sb, (it >> 1) & 1);
             }
-            // every softmax thread's rows are written: one release (cumulative
-            // over the barrier) and one arrival on the peer's barrier
-            if (named_sync_or(1, 256, !okw)) {
-                failed = true;
-                break;
-            }
-            if (tid == 128) {
-                fence_acq_rel_cluster();
-                mbar_arrive_cluster_relaxed(mapa_shared(bar(B_XF + sb), peer));
-            }
-            okw = __all_sync(0xffffffffu, wbc(B_XF + sb, (it >> 1) & 1));
+            okw = __all_sync(0xffffffffu, okw);
             float s[32];
             if (okw) {
                 const float4 *src = sX + ((sb * 2 + h) * 8) * kRows + r;
@@ -358,9 +353,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 break;
             }
             if (tid == 128) {
-                // every softmax thread has read the peer's rows: our buffer sb is
-                // free again (one release and one arrival for all of them)
-                fence_acq_rel_cluster();
+                // every softmax thread has read the peer's rows (their values fed
+                // the barrier above): our buffer sb is free again
                 mbar_arrive_cluster_relaxed(mapa_shared(bar(B_XE + sb), peer));
             }
             const float tmax = __fmul_rn(fmaxf(xmax[r], xmax[kRows + r]), p.scale_log2);

@@ -285,6 +285,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return r;
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory whose bytes
+// are counted on that CTA's mbarrier (complete_tx): the receiver's wait on the
+// barrier sees the data without any fence on this side.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
