@@ -55,7 +55,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     constexpr uint32_t ID_PV = idesc_bf16_f32(kRows, kHalfCols, true);
     constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
     constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_XF = B_PV + 2, B_XE = B_XF + 2;
-    constexpr int B_FIN = B_XE + 2, B_PROD = B_FIN + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
+    constexpr int B_XS = B_XE + 2;  // the sending warps have read S of this buffer
+    constexpr int B_FIN = B_XS + 2, B_PROD = B_FIN + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
     // launched with programmatic stream serialization: no global read before
@@ -132,6 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             mbar_init(bar(B_PV + i), 1);
             mbar_init(bar(B_XF + i), 1);  // armed here each tile; the peer's rows land as its bytes
             mbar_init(bar(B_XE + i), 1);  // the peer's softmax threads have read what we wrote
+            mbar_init(bar(B_XS + i), 4);  // the four sending warps
         }
         mbar_init(bar(B_FIN), 8);
         mbar_init(bar(B_PROD), 1);
@@ -268,6 +270,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 const int sk = it % NSK;
                 if (lane == 0) {
                     ok = wb(B_KF + sk, (it / NSK) & 1);
+                    // S buffer it & 1 was last read by the sending warps for tile it - 2
+                    if (ok && it >= 2)
+                        ok = wb(B_XS + (it & 1), ((it >> 1) - 1) & 1);
                     if (ok) {
                         tc_fence_after();
                         const uint32_t kbase = smem_addr(sK + sk * kTileBytes);
@@ -307,24 +312,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
         for (int it = 0; it < n_it; ++it) {
             const int sb = it & 1;
             // own partial S -> the peer's exchange buffer, then the peer's -> ours
+            // own partial S from tensor memory, the peer's from the exchange
+            // buffer (sent by the peer's sending warps, a tile ahead)
             bool okw = !failed && wb(B_SF + sb, (it >> 1) & 1);
-            if (okw && it >= 2)
-                okw = wbc(B_XE + sb, ((it >> 1) - 1) & 1);  // the peer has read what we wrote two tiles ago
             okw = __all_sync(0xffffffffu, okw);
             tc_fence_after();
             const uint32_t scol = tmem + lane_off + kSCol + sb * kKeys + 32 * h;
             uint32_t v[32];
             if (okw) {
-                // this tile's incoming rows: 32 KB from the peer's st.async
-                if (tid == 128)
-                    mbar_arrive_expect_tx(bar(B_XF + sb), kXBytes);
                 tmem_ld32(scol, v);
                 tmem_wait_ld();
-                const uint32_t dst = mapa_shared(smem_addr(sX + ((sb * 2 + h) * 8) * kRows + r), peer);
-                const uint32_t rbar = mapa_shared(bar(B_XF + sb), peer);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    st_async_v4(dst + i * kRows * 16, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], rbar);
                 okw = wbc(B_XF + sb, (it >> 1) & 1);
             }
             okw = __all_sync(0xffffffffu, okw);
@@ -431,7 +428,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             }
         }
     } else if (warp >= 12) {
-        // ------------------------------------ Q into TMEM, then epilogue --
+        // ------------------- Q into TMEM, the score sending, then epilogue --
         const int q4 = warp % 4;
         const int r = q4 * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
@@ -461,6 +458,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(B_Q));
+        }
+        // ------------------------------------------------ sending warps --
+        // This CTA's partial scores of tile it (both 32-column halves of row
+        // r) into the peer's exchange buffer with st.async, as soon as Q.K^T
+        // (it) is done and the peer has read what was sent two tiles ago;
+        // the bytes complete the transaction count of the peer's barrier,
+        // which this side's thread 384 arms for the incoming rows of the same
+        // tile.  The softmax of a tile thus finds the peer's rows waiting.
+        for (int it = 0; it < n_it; ++it) {
+            const int sb = it & 1;
+            bool okx = wb(B_SF + sb, (it >> 1) & 1);
+            if (okx && it >= 2)
+                okx = wbc(B_XE + sb, ((it >> 1) - 1) & 1);
+            if (!__all_sync(0xffffffffu, okx))
+                break;
+            if (tid == 384)
+                mbar_arrive_expect_tx(bar(B_XF + sb), kXBytes);
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_off + kSCol + sb * kKeys, v0);
+            tmem_ld32(tmem + lane_off + kSCol + sb * kKeys + 32, v1);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_XS + sb));  // Q.K^T(it + 2) may overwrite this S buffer
+            const uint32_t rbar = mapa_shared(bar(B_XF + sb), peer);
+            const uint32_t d0 = mapa_shared(smem_addr(sX + ((sb * 2) * 8) * kRows + r), peer);
+            const uint32_t d1 = mapa_shared(smem_addr(sX + ((sb * 2 + 1) * 8) * kRows + r), peer);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                st_async_v4(d0 + i * kRows * 16, v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3], rbar);
+                st_async_v4(d1 + i * kRows * 16, v1[4 * i], v1[4 * i + 1], v1[4 * i + 2], v1[4 * i + 3], rbar);
+            }
         }
         bool ok = wb(B_FIN, 0);
         if (ok)
