@@ -297,13 +297,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                  : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
 // Arrive on an mbarrier of another CTA in the cluster; orders this thread's
 // earlier writes (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
@@ -316,10 +309,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 // thread's memory writes (relaxed).  For hand-offs of tensor memory, whose
 // order is given by tcgen05.wait + tcgen05.fence::before_thread_sync, and of
 // pure counts.
-// Release fence at cluster scope: this thread's earlier memory operations,
-// and those ordered before it by a barrier, before its later ones.
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
