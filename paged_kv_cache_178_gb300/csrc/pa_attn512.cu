@@ -114,7 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
         const int pg = t * 4 + lane;
         return (lane < 8 && pg < npages_need) ? __ldg(bt_row + pg) : 0;
     };
-    int ids_cur = (warp == 0) ? load8(0) : 0;
+    int ids_cur = (warp == 0 || warp == 2) ? load8(0) : 0;
 
     // -------------------------------------------------------------- setup --
     if (tid == 0) {
@@ -155,12 +155,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     tc_fence_after();
     const uint32_t tmem = static_cast<uint32_t>(sflags[1]);
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer --
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------- producers: K (warp 0), V (warp 2) --
+        // One warp per operand: a K tile is issued as soon as its stage is
+        // free, not behind the V load of the tile before (which waits for the
+        // P.V of two tiles back).  Both warps read the block ids; warp 0
+        // reports bad ones.
+        static_assert(NSK == NSV, "one stage count for both producers");
+        constexpr int NS = NSK;
+        const bool is_v = warp == 2;
+        const int B_F = is_v ? B_VF : B_KF, B_E = is_v ? B_VE : B_KE;
+        const CUtensorMap *tm = is_v ? &p.tm_v : &p.tm_k;
+        uint8_t *const sbase = is_v ? sV : sK;
         bool ok = true, any_bad = false;
-        int last_k_use[NSK], last_v_use[NSV];
-        for (int s = 0; s < NSK; ++s) last_k_use[s] = -1;
-        for (int s = 0; s < NSV; ++s) last_v_use[s] = -1;
+        int last_use[NS];
+        for (int s = 0; s < NS; ++s) last_use[s] = -1;
         int ids_next = 0;
         for (int it = 0; ok && it < n_it; ++it) {
             if ((it & 1) == 0) {
@@ -179,49 +188,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             const int my_id = __shfl_sync(0xffffffffu, id, my_page & 3);
             const bool issue = lane < np * kNKB;
             const int col = (int)crank * kHalfCols + my_kb * 64;
-            const int sk = it % NSK, uk = it / NSK;
+            const int st = it % NS, use = it / NS;
             if (lane == 0) {
-                if (uk >= 1)
-                    ok = wb(B_KE + sk, (uk - 1) & 1);
+                if (use >= 1)
+                    ok = wb(B_E + st, (use - 1) & 1);
                 if (ok)
-                    mbar_arrive_expect_tx(bar(B_KF + sk), np * kNKB * 2048);
+                    mbar_arrive_expect_tx(bar(B_F + st), np * kNKB * 2048);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok)
                 break;
             if (issue)
-                tma_load_4d(smem_addr(sK + sk * kTileBytes + my_kb * 8192 + my_page * 2048), &p.tm_k,
-                            bar(B_KF + sk), col, kvh, 0, my_id);
-            last_k_use[sk] = uk;
-            const int sv = it % NSV, uv = it / NSV;
-            if (lane == 0) {
-                if (uv >= 1)
-                    ok = wb(B_VE + sv, (uv - 1) & 1);
-                if (ok)
-                    mbar_arrive_expect_tx(bar(B_VF + sv), np * kNKB * 2048);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok)
-                break;
-            if (issue)
-                tma_load_4d(smem_addr(sV + sv * kTileBytes + my_kb * 8192 + my_page * 2048), &p.tm_v,
-                            bar(B_VF + sv), col, kvh, 0, my_id);
-            last_v_use[sv] = uv;
+                tma_load_4d(smem_addr(sbase + st * kTileBytes + my_kb * 8192 + my_page * 2048), tm, bar(B_F + st),
+                            col, kvh, 0, my_id);
+            last_use[st] = use;
         }
         if (lane == 0) {
-            if (any_bad) {
-                record_error(p.err, kErrBadMetadata, b);
-                sflags[3] = 1;
+            if (!is_v) {
+                if (any_bad) {
+                    record_error(p.err, kErrBadMetadata, b);
+                    sflags[3] = 1;
+                }
+                mbar_arrive(bar(B_PROD));
             }
-            mbar_arrive(bar(B_PROD));
-            if (!ok) {
-                for (int s = 0; s < NSK; ++s)
-                    if (last_k_use[s] >= 0)
-                        wait_bar_drain(bar(B_KF + s), last_k_use[s] & 1);
-                for (int s = 0; s < NSV; ++s)
-                    if (last_v_use[s] >= 0)
-                        wait_bar_drain(bar(B_VF + s), last_v_use[s] & 1);
-            }
+            if (!ok)
+                for (int s = 0; s < NS; ++s)
+                    if (last_use[s] >= 0)
+                        wait_bar_drain(bar(B_F + s), last_use[s] & 1);
         }
         __syncwarp();
     } else if (warp == 1) {

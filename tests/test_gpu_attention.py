@@ -385,6 +385,41 @@ def test_wide_head_prefill_equals_decode(L, nrows):
     _prefill_vs_decode(w, rows)
 
 
+@pytest.mark.parametrize("bad_page", ["first", "last"])
+def test_wide_head_bad_block_id(bad_page):
+    """Dh=512, two prefill requests: a block id past the pool in request 1
+    latches the error for request 1; request 0 is bitwise unchanged.  With
+    the bad id on the first page every row of request 1 reads it and is NaN;
+    on the last page the rows whose keys reach it are NaN and every other row
+    of request 1 is either wholly NaN or bitwise the clean result."""
+    lens = (300, 200)
+    g = torch.Generator().manual_seed(512)
+    pages = torch.randperm(64, generator=g).tolist()
+    n0 = wl.pages_needed(lens[0])
+    rows = [pages[:n0], pages[n0:n0 + wl.pages_needed(lens[1])]]
+    w = wl.build("wide_two_requests", num_q_heads=16, num_kv_heads=2, head_dim=512, seq_lens=list(lens),
+                 query_lens=list(lens), num_blocks=64, block_rows=rows, layout="interleaved", seed=5120)
+    dw, out, lse = _run(w)
+    assert "in-cta-pair" in pagedattn.last_launch_info()
+    _compare(w, out, lse, rows=[0, 1, 150, 299, 300, 301, 420, 499])
+    bt = dw.block_tables.clone()
+    col = 0 if bad_page == "first" else len(rows[1]) - 1
+    bt[1, col] = w.num_blocks + 3
+    o2, l2 = dw.attention(block_tables=bt)
+    st, idx = pagedattn.check_errors()
+    assert st == pagedattn.PA_ERR_BAD_METADATA and idx == 1
+    _bitwise(out[:lens[0]], o2[:lens[0]], "request 0 beside a bad block id")
+    _bitwise(lse[:lens[0]], l2[:lens[0]], "request 0 lse beside a bad block id")
+    r1, l1 = o2[lens[0]:].float(), l2[lens[0]:]
+    nan_rows = torch.isnan(r1).flatten(1).all(1) & torch.isnan(l1).all(1)
+    reaches = torch.arange(lens[1], device=r1.device) >= 16 * col
+    assert bool(nan_rows[reaches].all())
+    clean = ~nan_rows
+    assert not bool(torch.isnan(r1[clean]).any())
+    _bitwise(out[lens[0]:][clean], o2[lens[0]:][clean], "request 1 rows clear of the bad page")
+    print(f"bad {bad_page} page: {int(nan_rows.sum())} of {lens[1]} rows NaN")
+
+
 def test_composition_prefill_equals_decode_all_rows():
     """The Dh=256 composition (20 tokens, table {3,1,2,0}): each of the 20
     prefill rows equals its decode view bit for bit."""
