@@ -11,7 +11,12 @@
 //     reads the peer's, then both form S = S_0 + S_1 (IEEE addition is
 //     commutative, so both CTAs hold the same bits) and run the identical
 //     softmax, so P, m and l agree bit for bit across the pair;
-//   - O_c += P . V_c (N = 256) accumulates in the CTA's own TMEM.
+//   - P (BF16) goes to one shared-memory buffer in the K-major swizzled
+//     layout of an MMA operand, and O_c += P . V_c (N = 256, both operands
+//     from shared memory) accumulates in the CTA's own TMEM.  With P out of
+//     the S buffers, Q.K^T of tile j + 2 may start as soon as S of tile j has
+//     been read, two tiles ahead of P.V, so the score exchange of a tile
+//     overlaps the softmax of the tile before.
 // Warp roles and the fixed arithmetic follow the head-dim 128/256 kernel,
 // with KV tiles of 64 keys (C1 at head dim 512) and 32-column softmax halves:
 //   tile sum = (8-way interleaved sum of the half's 32 columns) for each half,
@@ -34,14 +39,15 @@ constexpr int kStagesK = 2, kStagesV = 2;
 // columns][128 rows] of float4, so the 16-byte stores of a warp's 32 rows
 // into the peer (and their loads here) cover 512 contiguous bytes
 constexpr int kXBytes = 2 * 8 * kRows * 16;
+constexpr int kPBytes = kRows * kKeys * 2;  // P of one tile: 128 rows x 64 keys, BF16
 constexpr int kSmallBytes = 512 + 64 + 2 * 2 * kRows * 4 + kRows * 2 * 4;
 constexpr uint32_t kQCol = 0;           // TMEM: Q half (128 columns of BF16 pairs)
-constexpr uint32_t kSCol = 128;         // TMEM: two S/P buffers of 64 columns
+constexpr uint32_t kSCol = 128;         // TMEM: two S buffers of 64 columns
 constexpr uint32_t kOCol = 256;         // TMEM: O half (256 columns)
 
 constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)kTileBytes * (kStagesK + kStagesV) + 2 * (size_t)kXBytes + kSmallBytes;
+    return 1024 + (size_t)kTileBytes * (kStagesK + kStagesV) + 2 * (size_t)kXBytes + kPBytes + kSmallBytes;
 }
 
 }  // namespace d512
@@ -55,7 +61,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     constexpr uint32_t ID_PV = idesc_bf16_f32(kRows, kHalfCols, true);
     constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NSK, B_VF = B_KE + NSK, B_VE = B_VF + NSV;
     constexpr int B_SF = B_VE + NSV, B_PF = B_SF + 2, B_PV = B_PF + 2, B_XF = B_PV + 2, B_XE = B_XF + 2;
-    constexpr int B_XS = B_XE + 2;  // the sending warps have read S of this buffer
+    constexpr int B_XS = B_XE + 2;  // the sending and softmax warps have read S of this buffer
     constexpr int B_FIN = B_XS + 2, B_PROD = B_FIN + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
 
@@ -68,7 +74,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     uint8_t *sK = smem;
     uint8_t *sV = sK + NSK * kTileBytes;
     float4 *sX = reinterpret_cast<float4 *>(sV + NSV * kTileBytes);  // [2 S buffers][2 halves][8][128]
-    uint8_t *small = reinterpret_cast<uint8_t *>(sX) + 2 * kXBytes;
+    uint8_t *sP = reinterpret_cast<uint8_t *>(sX) + 2 * kXBytes;  // P, 8-row groups of 1024 bytes, swizzled
+    uint8_t *small = sP + kPBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(small);
     int *sflags = reinterpret_cast<int *>(small + 512);  // [0] abort [1] tmem [3] bad
     float *s_x = reinterpret_cast<float *>(small + 512 + 64);   // [2 exchanges][2 halves][128]
@@ -131,13 +138,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_PF + i), 8);
             mbar_init(bar(B_PV + i), 1);
-            mbar_init(bar(B_XF + i), 1);  // armed here each tile; the peer's rows land as its bytes
+            mbar_init(bar(B_XF + i), 1);  // armed for each tile; the peer's rows land as its bytes
             mbar_init(bar(B_XE + i), 1);  // the peer's softmax threads have read what we wrote
-            mbar_init(bar(B_XS + i), 4);  // the four sending warps
+            mbar_init(bar(B_XS + i), 12);  // the four sending warps and the eight softmax warps
         }
         mbar_init(bar(B_FIN), 8);
         mbar_init(bar(B_PROD), 1);
         mbar_init(bar(B_DONE), 1);
+        // the exchange buffers' first phases (tiles 0 and 1); each later
+        // phase is armed by the softmax once it has read the phase before
+        for (int i = 0; i < 2 && i < n_it; ++i)
+            mbar_arrive_expect_tx(bar(B_XF + i), kXBytes);
         sflags[0] = 0;
         sflags[3] = 0;
         fence_barrier_init();
@@ -245,12 +256,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 okj = wb(B_PF + (j & 1), (j >> 1) & 1);
                 if (okj) {
                     tc_fence_after();
-                    const uint32_t pcol = tmem + kSCol + (uint32_t)(j & 1) * kKeys;
+                    const uint32_t pbase = smem_addr(sP);
                     const uint32_t vbase = smem_addr(sV + sv * kTileBytes);
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        const uint64_t ad = sdesc_sw128(pbase + kk * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(vbase + kk * 2048, 8192, 1024);
-                        mma_bf16_ts(tmem + kOCol, pcol + kk * 8, bd, ID_PV, (kk > 0 || j > 0) ? 1u : 0u);
+                        mma_bf16_ss(tmem + kOCol, ad, bd, ID_PV, (kk > 0 || j > 0) ? 1u : 0u);
                     }
                     mma_commit(bar(B_VE + sv));
                     mma_commit(bar(B_PV + (j & 1)));
@@ -258,12 +270,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             }
             return __shfl_sync(0xffffffffu, okj, 0);
         };
-        for (int it = 0; ok && it <= n_it; ++it) {
+        // Q.K^T(it), then P.V(it - 2): Q.K^T runs two tiles ahead
+        for (int it = 0; ok && it <= n_it + 1; ++it) {
             if (it < n_it) {
                 const int sk = it % NSK;
                 if (lane == 0) {
                     ok = wb(B_KF + sk, (it / NSK) & 1);
-                    // S buffer it & 1 was last read by the sending warps for tile it - 2
+                    // S buffer it & 1 was last read for tile it - 2 (sending and softmax warps)
                     if (ok && it >= 2)
                         ok = wb(B_XS + (it & 1), ((it >> 1) - 1) & 1);
                     if (ok) {
@@ -281,8 +294,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
             }
-            if (ok && it >= 1)
-                ok = issue_pv(it - 1);
+            if (ok && it >= 2)
+                ok = issue_pv(it - 2);
         }
         if (lane == 0) {
             mma_commit(bar(B_DONE));
@@ -304,9 +317,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
         bool failed = false;
         for (int it = 0; it < n_it; ++it) {
             const int sb = it & 1;
-            // own partial S -> the peer's exchange buffer, then the peer's -> ours
-            // own partial S from tensor memory, the peer's from the exchange
-            // buffer (sent by the peer's sending warps, a tile ahead)
+            // own partial S from tensor memory (then the S buffer is released
+            // for Q.K^T two tiles on), the peer's from the exchange buffer
+            // (sent by the peer's sending warps as soon as its Q.K^T is done)
             bool okw = !failed && wb(B_SF + sb, (it >> 1) & 1);
             okw = __all_sync(0xffffffffu, okw);
             tc_fence_after();
@@ -315,8 +328,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             if (okw) {
                 tmem_ld32(scol, v);
                 tmem_wait_ld();
-                okw = wbc(B_XF + sb, (it >> 1) & 1);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (okw && lane == 0)
+                mbar_arrive(bar(B_XS + sb));
+            if (okw)
+                okw = wbc(B_XF + sb, (it >> 1) & 1);
             okw = __all_sync(0xffffffffu, okw);
             float s[32];
             if (okw) {
@@ -344,7 +362,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
             }
             if (tid == 128) {
                 // every softmax thread has read the peer's rows (their values fed
-                // the barrier above): our buffer sb is free again
+                // the barrier above): the buffer's barrier is armed for tile
+                // it + 2 (its phase of tile it is complete, so the arming falls
+                // in the next phase), then the buffer is handed back to the peer
+                if (it + 2 < n_it)
+                    mbar_arrive_expect_tx(bar(B_XF + sb), kXBytes);
                 mbar_arrive_cluster_relaxed(mapa_shared(bar(B_XE + sb), peer));
             }
             const float tmax = __fmul_rn(fmaxf(xmax[r], xmax[kRows + r]), p.scale_log2);
@@ -360,6 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 }
             }
             float hs = 0.f;
+            bool okp = true;
             if (warp_active) {
                 const float negm = -m_new;
                 float a[8];
@@ -379,18 +402,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 }
                 hs = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
                                __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
-                // P of keys [32h, 32h+32) -> columns [16h, 16h+16) of this S buffer
-                tmem_st16(tmem + lane_off + kSCol + sb * kKeys + 16 * h, w);
+                // the one P buffer was read by P.V(it - 1)
+                okp = it == 0 || __all_sync(0xffffffffu, wb(B_PV + ((it - 1) & 1), ((it - 1) >> 1) & 1));
+                // P of keys [32h, 32h+32): 16-byte chunks 4h..4h+3 of row r,
+                // swizzled by the row within its 8-row group
+                if (okp) {
+                    uint8_t *prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4 *>(prow + (((4 * h + q) ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    fence_proxy_async_smem();  // visible to the MMA's operand reads
+                }
             }
             xsum[h * kRows + r] = hs;
-            named_sync(1, 256);
-            const float tsum = __fadd_rn(xsum[r], xsum[kRows + r]);
-            bool okr = true;
-            if (__any_sync(0xffffffffu, need)) {
-                okr = __all_sync(0xffffffffu, wb(B_PV + ((it - 1) & 1), ((it - 1) >> 1) & 1));
-                failed = !okr;
+            if (named_sync_or(1, 256, !okp)) {
+                failed = true;
+                break;
             }
-            if (__any_sync(0xffffffffu, need) && okr) {
+            const float tsum = __fadd_rn(xsum[r], xsum[kRows + r]);
+            // O may be rescaled: P.V(it - 1) is complete (waited above by the
+            // active warps; an inactive warp never needs a rescale)
+            if (__any_sync(0xffffffffu, need)) {
                 tc_fence_after();
                 const float f = need ? corr : 1.f;
 #pragma unroll 1
@@ -457,8 +490,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
         // r) into the peer's exchange buffer with st.async, as soon as Q.K^T
         // (it) is done and the peer has read what was sent two tiles ago;
         // the bytes complete the transaction count of the peer's barrier,
-        // which this side's thread 384 arms for the incoming rows of the same
-        // tile.  The softmax of a tile thus finds the peer's rows waiting.
+        // which the peer's softmax armed when it released the buffer (the
+        // setup, for tiles 0 and 1).  The softmax of a tile thus finds the
+        // peer's rows waiting.
         for (int it = 0; it < n_it; ++it) {
             const int sb = it & 1;
             bool okx = wb(B_SF + sb, (it >> 1) & 1);
@@ -466,8 +500,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
                 okx = wbc(B_XE + sb, ((it >> 1) - 1) & 1);
             if (!__all_sync(0xffffffffu, okx))
                 break;
-            if (tid == 384)
-                mbar_arrive_expect_tx(bar(B_XF + sb), kXBytes);
             tc_fence_after();
             uint32_t v0[32], v1[32];
             tmem_ld32(tmem + lane_off + kSCol + sb * kKeys, v0);
