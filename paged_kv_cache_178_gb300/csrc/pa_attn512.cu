@@ -17,8 +17,15 @@
 //     the S buffers, Q.K^T of tile j + 2 may start as soon as S of tile j has
 //     been read, two tiles ahead of P.V, so the score exchange of a tile
 //     overlaps the softmax of the tile before.
-// Warp roles and the fixed arithmetic follow the head-dim 128/256 kernel,
-// with KV tiles of 64 keys (C1 at head dim 512) and 32-column softmax halves:
+// Warp roles (512 threads):
+//   warp 0       K producer: one 64-column box per 16-token page, this CTA's
+//                four column blocks, block ids range-checked as it goes
+//   warp 2       V producer, the same for V (K never waits behind a V load)
+//   warp 1       tcgen05 issuer: Q.K^T(it), then P.V(it - 2)
+//   warps 4-11   softmax, two 32-column halves, one TMEM lane (row) each
+//   warps 12-15  Q into TMEM, then the score sending, then the epilogue
+// The fixed arithmetic follows the head-dim 128/256 kernel, with KV tiles of
+// 64 keys (C1 at head dim 512) and 32-column softmax halves:
 //   tile sum = (8-way interleaved sum of the half's 32 columns) for each half,
 //   half0 + half1; one chunk per row (no split-KV at head dim 512).
 #include <cstdio>
