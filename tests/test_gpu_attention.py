@@ -385,6 +385,22 @@ def test_wide_head_prefill_equals_decode(L, nrows):
     _prefill_vs_decode(w, rows)
 
 
+def test_wide_head_suffix_prefill():
+    """Dh=512 suffix (chunked) prefill: two requests whose new tokens extend a
+    cached context (130 new on 700, 300 new on 300, tails mid-page and
+    mid-tile), against the oracle on rows of every query tile of both."""
+    lens, qlens = (700, 300), (130, 300)
+    g = torch.Generator().manual_seed(5121)
+    pages = torch.randperm(96, generator=g).tolist()
+    n0 = wl.pages_needed(lens[0])
+    rows = [pages[:n0], pages[n0:n0 + wl.pages_needed(lens[1])]]
+    w = wl.build("wide_suffix", num_q_heads=16, num_kv_heads=2, head_dim=512, seq_lens=list(lens),
+                 query_lens=list(qlens), num_blocks=96, block_rows=rows, layout="interleaved", seed=5122)
+    dw, out, lse = _run(w)
+    assert "in-cta-pair" in pagedattn.last_launch_info()
+    _compare(w, out, lse, rows=[0, 15, 16, 17, 63, 64, 100, 129, 130, 131, 146, 200, 300, 429])
+
+
 @pytest.mark.parametrize("bad_page", ["first", "last"])
 def test_wide_head_bad_block_id(bad_page):
     """Dh=512, two prefill requests: a block id past the pool in request 1
