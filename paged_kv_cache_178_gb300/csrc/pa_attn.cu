@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     constexpr int B_OF = B_CR + 2, B_PROD = B_OF + (OBUF2 ? 2 : 1), B_DONE = B_PROD + 1, B_VZ = B_DONE + 1;
     constexpr int NBARS = B_VZ + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
+    static_assert(smem_bytes<DH, PAIR, KT>() <= kMaxSmemPerBlock, "shared-memory layout");
 
     // Launched with programmatic stream serialization.  By default nothing
     // below reads global memory before the preceding grid of the stream has

@@ -71,6 +71,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512, 1) attn512_kern
     constexpr int B_XS = B_XE + 2;  // the sending and softmax warps have read S of this buffer
     constexpr int B_FIN = B_XS + 2, B_PROD = B_FIN + 1, B_DONE = B_PROD + 1, NBARS = B_DONE + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
+    static_assert(smem_bytes() <= kMaxSmemPerBlock, "shared-memory layout");
 
     // launched with programmatic stream serialization: no global read before
     // the preceding grid of the stream has completed

@@ -14,6 +14,9 @@ constexpr int kRows = 128;          // M of every MMA: rows per tile
 constexpr float kTau = 8.0f;        // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// Dynamic shared memory one CTA may opt into on sm_103a (227 KB); every
+// kernel's layout is checked against it at compile time.
+constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 struct AttnParams {
     CUtensorMap tm_q;
     CUtensorMap tm_k;

@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) dec_kernel(const __grid_cons
     constexpr int B_DONE = B_IDS + kBadRing, NBARS = B_DONE + 1;
     static_assert(NBARS * 8 <= 512, "barrier area");
     static_assert(R == 4 || R == 8 || R == 16 || R == 32, "rows per CTA");
+    static_assert(dec::smem_bytes<R>() <= kMaxSmemPerBlock, "shared-memory layout");
 
     // Launched with programmatic stream serialization (see pa_attn.cu): by
     // default nothing reads global memory before the preceding grid has
